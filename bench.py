@@ -1,0 +1,345 @@
+"""Benchmark: causal attention forward + backward TFLOP/s on one GB300.
+
+One step = dfa_attn_fwd followed by dfa_attn_bwd (from the saved O and lse)
+over one batch of seeded synthetic inputs of the chosen workload (default:
+the Llama-7B attention shape at 128K tokens, bf16).  FLOPs are algorithmic
+causal FLOPs: pairs = B*H*S(S+1)/2, 4D per pair forward and 10D per pair
+backward (P is recomputed from the saved lse), 14D per pair in total.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
+on a bounded sample of the same workload instead.
+
+Multi-GPU (torchrun): the path does not exchange data between GPUs; each rank
+runs its own batch of the workload (weak scaling) and the slowest rank's time
+is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+NOMINAL_BF16_TFLOPS = 2250.0
+DEFAULT_WORKLOAD = "llama7b_s128k"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["dfa", "reference"], default="dfa")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--sched", choices=["balanced", "unbalanced"], default="balanced")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target oracle sample time")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+def dist_setup(n_gpus):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- CPU oracle sample
+def oracle_sample(w, seconds, seed=0):
+    """Times the fp64 oracle on sampled query rows of workload `w`.
+
+    Returns (flops, elapsed_s, cores, description).  Each sampled row gets its
+    forward (O, lse: 4D FLOPs per visible key) and its dQ (recomputed scores,
+    dP and dQ: 6D per visible key)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from long_context_causal_gb300.inputs import make
+
+    # Inputs of one (batch, head) pair drawn with the workload's recipe; the
+    # oracle needs keys up to the sampled row only.
+    rng = np.random.default_rng(seed)
+    Hs = 1
+    Skv = w.S
+    q, k, v, do = make(1, Hs, 1, Skv, w.D, w.dtype, seed=w.seed, device="cpu", k_scale=w.k_scale)
+    f = lambda t: t.float().numpy().astype(np.float64)
+    q, k, v, do = f(q), f(k), f(v), f(do)
+    cores = oracle.num_threads()
+    # Calibrate: rows of average length S/2 cost ~10*D*S/2 FLOPs; aim for `seconds`.
+    rows_done, flops, elapsed = 0, 0.0, 0.0
+    batch = max(cores, 8)
+    while elapsed < seconds:
+        rows = np.sort(rng.integers(0, w.S, size=batch))
+        idx = np.stack([np.zeros_like(rows), np.zeros_like(rows), rows], axis=1)
+        t0 = time.perf_counter()
+        oracle.attn_fwd_rows(q, k, v, idx, scale=w.scale)
+        oracle.attn_dq_rows(q, k, v, do, idx, scale=w.scale)
+        elapsed += time.perf_counter() - t0
+        flops += float(np.sum(rows + 1)) * w.D * 10
+        rows_done += batch
+    desc = (f"{rows_done} random query rows of one head of {w.name} (S={w.S}, D={w.D}); "
+            f"forward O/lse and dQ per row in fp64")
+    return flops, elapsed, cores, desc
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    per_step = max(1.0, min(args.cpu_seconds, 180.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(w, per_step / 4, seed=1)
+    tot_f, tot_t, cores, desc = 0.0, 0.0, 1, ""
+    for s in range(args.steps):
+        fl, el, cores, desc = oracle_sample(w, per_step, seed=100 + s)
+        tot_f += fl
+        tot_t += el
+    val = tot_f / tot_t / 1e12
+    line = {
+        "impl": "reference", "metric": "causal attn fwd+bwd TFLOP/s (bf16, Llama-7B head shape)",
+        "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.H_kv, "S": w.S, "D": w.D,
+                   "n_chunks": w.n_chunks},
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+def main():
+    args = parse()
+    from long_context_causal_gb300.inputs import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    import torch
+
+    from long_context_causal_gb300 import dfa
+    from long_context_causal_gb300.inputs import make
+
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local if world > 1 else 0)
+    seed = w.seed + rank
+    q, k, v, do = make(w.B, w.H, w.H_kv, w.S, w.D, w.dtype, seed=seed, device=dev, k_scale=w.k_scale)
+    O = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
+    dQ, dK, dV = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    wsf = dfa.workspace(w.B, w.H, w.H_kv, w.S, w.D, w.n_chunks, False, dev)
+    wsb = dfa.workspace(w.B, w.H, w.H_kv, w.S, w.D, w.n_chunks, True, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        dfa.dfa_attn_fwd(q, k, v, n_chunks=w.n_chunks, scale=w.scale, sched=args.sched, O=O, lse=lse,
+                         workspace_buf=wsf, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        dfa.dfa_attn_bwd(q, k, v, O, lse, do, n_chunks=w.n_chunks, scale=w.scale, sched=args.sched,
+                         dQ=dQ, dK=dK, dV=dV, workspace_buf=wsb, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    dfa.dfa_check_errors(stream)
+
+    launches0 = sum(dfa.dfa_launch_count(kd) for kd in dfa.KERNEL_KINDS)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(local if world > 1 else 0) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.5)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(args.steps):
+        step(evs[s])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    dfa.dfa_check_errors(stream)
+    launches = sum(dfa.dfa_launch_count(kd) for kd in dfa.KERNEL_KINDS) - launches0
+
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    flops = w.causal_flops()
+    ms_step = total_ms / args.steps
+    value = world * flops / (ms_step * 1e-3) / 1e12
+
+    peaks, peak_kind = measured_peaks()
+    peak_tc = float(peaks["bf16_tflops"])
+    bwd_flops = w.causal_flops(fwd=False, bwd=True)
+    fwd_flops = w.causal_flops(fwd=True, bwd=False)
+    bwd_tflops = bwd_flops / (bwd_ms * 1e-3) / 1e12
+    fwd_tflops = fwd_flops / (fwd_ms * 1e-3) / 1e12
+
+    # End to end through the public API with host buffers: pinned host inputs are
+    # copied in, fwd + bwd run, and every result is copied back, inside the timing.
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, hdo = (t.cpu().pin_memory() for t in (q, k, v, do))
+        hO, hlse = torch.empty_like(hq).pin_memory(), torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        hdQ, hdK, hdV = (torch.empty_like(t).pin_memory() for t in (hq, hk, hv))
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+        d2h = sum(t.numel() * t.element_size() for t in (hO, hlse, hdQ, hdK, hdV))
+
+        def e2e_step():
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            do.copy_(hdo, non_blocking=True)
+            step()
+            hO.copy_(O, non_blocking=True)
+            hlse.copy_(lse, non_blocking=True)
+            hdQ.copy_(dQ, non_blocking=True)
+            hdK.copy_(dK, non_blocking=True)
+            hdV.copy_(dV, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        n_e2e = max(1, min(args.steps, 5))
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e2e_ms = max_over_ranks(a.elapsed_time(b), world) / n_e2e
+        e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": n_e2e}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        fl, el, cores, desc = oracle_sample(w, args.cpu_seconds)
+        cpu = {"value": fl / el / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": "causal attn fwd+bwd TFLOP/s (bf16, Llama-7B head shape)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype.is_floating_point and w.dtype.itemsize == 2 else "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.H_kv, "S": w.S, "D": w.D,
+                   "n_chunks": w.n_chunks, "sched": args.sched, "causal": True,
+                   "l2": "inputs larger than L2 (each tensor exceeds 129 MB)"},
+        "pct_of_nominal_bf16_peak": 100.0 * value / world / NOMINAL_BF16_TFLOPS,
+        "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
+        "roofline": {"bound": "tensor", "kernel": "dfa_attn_bwd (delta + bwd + dQ convert)",
+                     "achieved": bwd_tflops, "peak": peak_tc, "unit": "TFLOP/s",
+                     "frac": bwd_tflops / peak_tc, "traffic": None,
+                     "peak_kind": f"{peak_kind} bf16 burst"},
+        "roofline_fwd": {"bound": "tensor", "achieved": fwd_tflops, "peak": peak_tc, "unit": "TFLOP/s",
+                         "frac": fwd_tflops / peak_tc},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

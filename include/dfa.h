@@ -1,0 +1,165 @@
+/*
+ * dfa.h -- C ABI of the GB300 (sm_103a) causal chunk-attention library.
+ *
+ * The operation is the hot path of DISTFLASHATTN ("DISTFLASHATTN: Distributed
+ * Memory-efficient Attention for Long-context LLMs Training", paperlayer.ai
+ * summary of arXiv 2310.03294): exact causal softmax attention over a
+ * sequence split into P token chunks.  Each query chunk attends to the
+ * key/value chunks at or before it (§3.2), each chunk step returns a partial
+ * output with its log-sum-exp (App. D), partials combine with the
+ * online-softmax rescale-and-merge rule (§3.2), and the backward reuses the
+ * saved output and log-sum-exp so the forward is never recomputed (§3.3).
+ *
+ * Mathematical definition (natural-log lse, scale applied to the scores):
+ *   s_ij = scale * <q_i, k_j>, visible iff !causal or kv_pos(j) <= q_pos(i)
+ *   lse_i = ln sum_j exp(s_ij),  O_i = sum_j exp(s_ij - lse_i) v_j
+ * A row with no visible key has O_i = 0 and lse_i = -inf.  Grouped-query
+ * attention: query head h reads key/value head h / (H / H_kv).
+ *
+ * Conventions shared by every entry point
+ *  - Layouts: Q, O, dO, dQ are [B, S, H, D]; K, V, dK, dV are [B, S, H_kv, D]
+ *    (BSHD, D contiguous); lse and Delta are fp32 [B, H, S] contiguous.
+ *  - Every pointer is a DEVICE pointer owned by the caller; the library never
+ *    allocates device memory.  `stream` is a cudaStream_t (NULL = legacy default).
+ *  - Calls are asynchronous on `stream`: DFA_OK means "validated and launched".
+ *    A kernel that gives up on a bounded wait sets a device error flag that
+ *    dfa_check_errors() reports as DFA_ERR_TIMEOUT.
+ *  - No exception crosses this boundary.  On a non-OK status nothing was
+ *    launched and dfa_last_error() holds a message (thread-local).
+ *  - dtype: DFA_BF16 runs the tcgen05 tensor-core kernels (fp32 accumulation);
+ *    DFA_F32 runs fp32 CUDA-core kernels (fp32 I/O needs more than one-pass
+ *    tf32 accuracy).  O, dO, dQ, dK and dV share the input dtype.
+ *  - Supported head dims: D in {64, 128}.  Pointers must be 16-byte aligned.
+ */
+#ifndef DFA_H
+#define DFA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DFA_OK = 0,
+    DFA_ERR_INVALID_ARG = 1,   /* bad pointer, size, stride, alignment or scale   */
+    DFA_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement     */
+    DFA_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed            */
+    DFA_ERR_TIMEOUT = 4,       /* a kernel gave up on a bounded wait              */
+    DFA_ERR_WORKSPACE = 5      /* workspace missing or smaller than required      */
+} dfa_status;
+
+typedef enum { DFA_F32 = 0, DFA_BF16 = 1 } dfa_dtype;
+
+/* Work distribution over persistent CTAs (DISTFLASHATTN §3.2 and App. B).
+ * UNBALANCED: the pages' baseline -- the sequence is cut into one contiguous
+ *   token range per worker (CTA) and each worker computes its causal prefix,
+ *   so late workers carry most of the triangle.
+ * BALANCED: the token-level balanced schedule -- a worker that takes an
+ *   early (cheap) query tile also takes its mirror image at the end of the
+ *   sequence, and these equal-cost pairs are dealt to the workers in turn,
+ *   so every worker gets the same amount of work to within one pair. */
+typedef enum { DFA_SCHED_BALANCED = 0, DFA_SCHED_UNBALANCED = 1 } dfa_sched;
+
+/* One chunk step (DISTFLASHATTN App. D: "update the attention state, return
+ * the output and its log-sum-exp"): a query chunk of Lq rows at global
+ * position q_offset against a key/value chunk of Lkv rows at kv_offset.
+ *   q:        [B, Lq, H, D] with element strides q_strides = {batch, seq, head}
+ *   k, v:     [B, Lkv, H_kv, D] with element strides kv_strides (shared by k, v)
+ *             (either stride array may be NULL for the dense layout; strides
+ *             must be multiples of 8 elements so rows stay 16-byte aligned)
+ *   causal:   1 = mask kv_offset + j > q_offset + i; 0 = attend to the whole chunk
+ *   O_partial: fp32 [B, Lq, H, D] dense, the normalised partial output
+ *   lse:      fp32 [B, H, Lq] dense, natural-log log-sum-exp of the partial
+ * Rows that see no key of this chunk get O_partial = 0 and lse = -inf. */
+dfa_status dfa_chunk_attn_fwd(const void* q, const void* k, const void* v, dfa_dtype dt,
+                              int B, int H, int H_kv, int Lq, int Lkv, int D,
+                              const int64_t* q_strides, const int64_t* kv_strides,
+                              int64_t q_offset, int64_t kv_offset, int causal, float scale,
+                              float* O_partial, float* lse, void* stream);
+
+/* Online-softmax rescale-and-merge of two partials over the same rows
+ * (DISTFLASHATTN §3.2: helpers return partial outputs plus softmax statistics
+ * that the owner rescales):
+ *   lse = ln(e^lse_a + e^lse_b),  O = e^(lse_a - lse) O_a + e^(lse_b - lse) O_b.
+ * A partial with lse = -inf has weight 0; both -inf gives O = 0, lse = -inf.
+ *   O_a, O_b, O_out: fp32 [B, L, H, D];  lse_a, lse_b, lse_out: fp32 [B, H, L].
+ * O_out may alias O_a or O_b, lse_out may alias lse_a or lse_b. */
+dfa_status dfa_merge_partials(int B, int H, int L, int D,
+                              const float* O_a, const float* lse_a,
+                              const float* O_b, const float* lse_b,
+                              float* O_out, float* lse_out, void* stream);
+
+/* Bytes of workspace dfa_attn_fwd (bwd = 0) or dfa_attn_bwd (bwd = 1) needs.
+ * Returns 0 for invalid sizes. */
+size_t dfa_attn_workspace_size(int B, int H, int H_kv, int S, int D, int n_chunks, int bwd);
+
+/* Whole-sequence causal forward over n_chunks token chunks (DISTFLASHATTN §3.1,
+ * §3.2).  Chunk partials of one query tile are merged on chip with the
+ * rescale-and-merge rule as the key/value chunks stream by, so the result
+ * equals the monolithic softmax up to rounding.
+ *   q: [B, S, H, D], k, v: [B, S, H_kv, D] dense;  O: [B, S, H, D] in dt;
+ *   lse: fp32 [B, H, S] (saved for the backward).  S % n_chunks == 0. */
+dfa_status dfa_attn_fwd(const void* q, const void* k, const void* v, dfa_dtype dt,
+                        int B, int H, int H_kv, int S, int D, int n_chunks, int causal,
+                        float scale, dfa_sched sched, void* O, float* lse,
+                        void* workspace, size_t ws_bytes, void* stream);
+
+/* Backward from the SAVED O and lse (DISTFLASHATTN §3.3, rematerialization-aware
+ * checkpointing: the forward is computed once and never re-run here):
+ *   Delta_i = <dO_i, O_i>,  P_ij = exp(s_ij - lse_i),  dS_ij = P_ij (dO_i.v_j - Delta_i)
+ *   dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO  (dK, dV summed over a GQA group).
+ * Same layouts as dfa_attn_fwd; dQ/dK/dV are written (not accumulated) in dt.
+ * The workspace holds the fp32 dQ accumulator and Delta. */
+dfa_status dfa_attn_bwd(const void* q, const void* k, const void* v, const void* O,
+                        const float* lse, const void* dO, dfa_dtype dt,
+                        int B, int H, int H_kv, int S, int D, int n_chunks, int causal,
+                        float scale, dfa_sched sched, void* dQ, void* dK, void* dV,
+                        void* workspace, size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, then reports and clears the device error flag:
+ * DFA_ERR_TIMEOUT if a kernel gave up on a bounded wait, DFA_ERR_CUDA if the
+ * stream holds a CUDA error, DFA_OK otherwise. */
+dfa_status dfa_check_errors(void* stream);
+
+/* Message for the last non-OK status returned on this thread ("" if none). */
+const char* dfa_last_error(void);
+
+/* Kernel launches issued by this process, per kind (host-side counters,
+ * incremented when a launch is enqueued).  Lets callers verify, for example,
+ * that dfa_attn_bwd never launches a forward kernel. */
+typedef enum {
+    DFA_KERNEL_FWD = 0,       /* attention forward (tensor-core or fp32)   */
+    DFA_KERNEL_BWD = 1,       /* attention backward main kernel(s)         */
+    DFA_KERNEL_MERGE = 2,     /* partial rescale-and-merge                 */
+    DFA_KERNEL_DELTA = 3,     /* Delta = rowsum(dO * O) preprocessing      */
+    DFA_KERNEL_CONVERT = 4,   /* fp32 dQ accumulator -> output dtype       */
+    DFA_KERNEL_KINDS = 5
+} dfa_kernel_kind;
+int64_t dfa_launch_count(dfa_kernel_kind kind);
+
+/* ---- host-only scheduling helpers (no GPU needed; used by the tests) ---- */
+
+/* Builds the persistent-CTA work list for `n_units` units of causal work per
+ * (batch, head) row of `n_rows` rows, unit u costing (u + 1) key/value tiles.
+ * Writes per-worker item ranges into offsets[n_workers + 1] and the unit
+ * indices into items[n_rows * n_units] as (row * n_units + u), in the order
+ * each worker processes them.  Returns the makespan in tiles (the largest
+ * per-worker cost) or -1 on bad arguments. */
+int64_t dfa_build_worklist(int n_rows, int n_units, int n_workers, dfa_sched sched,
+                           int32_t* offsets, int32_t* items);
+
+/* The pages' distributed schedule at chunk-step granularity (DISTFLASHATTN
+ * App. B, Figs. 5-6, and §4.5): P workers own one chunk each, a step computes
+ * one (query chunk, key/value chunk) block per worker.  Writes for each step s
+ * and worker w the block it computes as (qchunk * P + kvchunk), or -1 if idle,
+ * into steps[s * P + w] (capacity max_steps * P).  Returns the number of
+ * steps (the makespan), or -1 on bad arguments / insufficient capacity. */
+int dfa_chunk_schedule(int P, dfa_sched sched, int max_steps, int32_t* steps);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFA_H */

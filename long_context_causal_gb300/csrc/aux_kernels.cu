@@ -1,0 +1,163 @@
+// aux_kernels.cu -- HBM-bound helper kernels of the attention path.
+//
+//  * merge:   the online-softmax rescale-and-merge of two partial results
+//             (DISTFLASHATTN §3.2, paperlayer.ai summary of arXiv 2310.03294:
+//             helpers return partial outputs plus softmax statistics that the
+//             owner rescales before combining);
+//  * delta:   Delta_i = <dO_i, O_i>, the per-row term of the softmax gradient,
+//             read once from the SAVED output (§3.3: the backward reuses the
+//             forward's output instead of recomputing it);
+//  * convert: the fp32 dQ accumulator scaled and cast to the output dtype.
+// Each is a streaming pass: one warp per row, 16-byte loads, no reuse.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "internal.h"
+
+namespace dfa {
+namespace {
+
+constexpr int kThreads = 256;
+
+__global__ void __launch_bounds__(kThreads)
+merge_kernel(int B, int H, int L, int D, const float* Oa, const float* la, const float* Ob,
+             const float* lb, float* O, float* l) {
+    const int64_t row = (int64_t)blockIdx.x * (kThreads / 32) + threadIdx.x / 32;  // (b, i, h)
+    const int lane = threadIdx.x % 32;
+    if (row >= (int64_t)B * L * H) return;
+    const int h = row % H;
+    const int64_t bi = row / H;
+    const int i = bi % L, b = bi / L;
+    const int64_t li = ((int64_t)b * H + h) * L + i;
+    const float a = la[li], c = lb[li];
+    const float m = fmaxf(a, c);
+    float wa = 0.f, wc = 0.f, lse = -INFINITY;
+    if (m != -INFINITY) {
+        const float ea = expf(a - m), ec = expf(c - m);
+        const float sum = ea + ec;
+        lse = m + logf(sum);
+        wa = ea / sum;
+        wc = ec / sum;
+    }
+    const float4* pa = reinterpret_cast<const float4*>(Oa + row * D);
+    const float4* pb = reinterpret_cast<const float4*>(Ob + row * D);
+    float4* po = reinterpret_cast<float4*>(O + row * D);
+    for (int x = lane; x < D / 4; x += 32) {
+        const float4 u = pa[x], w = pb[x];
+        po[x] = make_float4(wa * u.x + wc * w.x, wa * u.y + wc * w.y, wa * u.z + wc * w.z,
+                            wa * u.w + wc * w.w);
+    }
+    __syncwarp();
+    if (lane == 0) l[li] = lse;
+}
+
+template <typename T>
+__device__ __forceinline__ void load8(const T* p, float* out);
+template <>
+__device__ __forceinline__ void load8<float>(const float* p, float* out) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+    out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
+    out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
+}
+template <>
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float* out) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+        const float2 f = __bfloat1622float2(h[x]);
+        out[2 * x] = f.x;
+        out[2 * x + 1] = f.y;
+    }
+}
+
+// One warp per (b, i, h) row; D / 8 lanes each read 8 elements.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+delta_kernel(int B, int H, int S, int D, const T* __restrict__ O, const T* __restrict__ dO,
+             float* __restrict__ delta) {
+    const int64_t row = (int64_t)blockIdx.x * (kThreads / 32) + threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    if (row >= (int64_t)B * S * H) return;
+    float acc = 0.f;
+    for (int x = lane; x < D / 8; x += 32) {
+        float a[8], c[8];
+        load8<T>(O + row * D + 8 * x, a);
+        load8<T>(dO + row * D + 8 * x, c);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc = fmaf(a[e], c[e], acc);
+    }
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) {
+        const int h = row % H;
+        const int64_t bi = row / H;
+        const int i = bi % S, b = bi / S;
+        delta[((int64_t)b * H + h) * S + i] = acc;
+    }
+}
+
+__global__ void convert_bf16_kernel(int64_t n, float scale, const float* __restrict__ in,
+                                    __nv_bfloat16* __restrict__ out) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < n / 8; x += stride) {
+        const float4 a = reinterpret_cast<const float4*>(in)[2 * x];
+        const float4 b = reinterpret_cast<const float4*>(in)[2 * x + 1];
+        __nv_bfloat162 r[4] = {__floats2bfloat162_rn(scale * a.x, scale * a.y),
+                               __floats2bfloat162_rn(scale * a.z, scale * a.w),
+                               __floats2bfloat162_rn(scale * b.x, scale * b.y),
+                               __floats2bfloat162_rn(scale * b.z, scale * b.w)};
+        reinterpret_cast<uint4*>(out)[x] = *reinterpret_cast<uint4*>(r);
+    }
+}
+
+__global__ void convert_f32_kernel(int64_t n, float scale, const float* __restrict__ in,
+                                   float* __restrict__ out) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < n; x += stride)
+        out[x] = scale * in[x];
+}
+
+dfa_status launched(const char* what) {
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? DFA_OK : fail(DFA_ERR_CUDA, "%s launch: %s", what, cudaGetErrorString(e));
+}
+
+}  // namespace
+
+dfa_status launch_merge(int B, int H, int L, int D, const float* Oa, const float* la,
+                        const float* Ob, const float* lb, float* O, float* l, cudaStream_t s) {
+    const int64_t rows = (int64_t)B * L * H;
+    if (rows == 0) return DFA_OK;
+    const int64_t blocks = (rows + kThreads / 32 - 1) / (kThreads / 32);
+    merge_kernel<<<(unsigned)blocks, kThreads, 0, s>>>(B, H, L, D, Oa, la, Ob, lb, O, l);
+    return launched("merge");
+}
+
+dfa_status launch_delta(dfa_dtype dt, int B, int H, int S, int D, const void* O,
+                        const void* dO, float* delta, cudaStream_t s) {
+    const int64_t rows = (int64_t)B * S * H;
+    if (rows == 0) return DFA_OK;
+    const int64_t blocks = (rows + kThreads / 32 - 1) / (kThreads / 32);
+    if (dt == DFA_F32)
+        delta_kernel<float><<<(unsigned)blocks, kThreads, 0, s>>>(B, H, S, D, (const float*)O,
+                                                                  (const float*)dO, delta);
+    else
+        delta_kernel<__nv_bfloat16><<<(unsigned)blocks, kThreads, 0, s>>>(
+            B, H, S, D, (const __nv_bfloat16*)O, (const __nv_bfloat16*)dO, delta);
+    return launched("delta");
+}
+
+dfa_status launch_convert(dfa_dtype dt, int64_t n, float scale, const float* acc, void* out,
+                          cudaStream_t s) {
+    if (n == 0) return DFA_OK;
+    const int blocks = 8 * num_sms();
+    if (dt == DFA_BF16)
+        convert_bf16_kernel<<<blocks, kThreads, 0, s>>>(n, scale, acc, (__nv_bfloat16*)out);
+    else
+        convert_f32_kernel<<<blocks, kThreads, 0, s>>>(n, scale, acc, (float*)out);
+    return launched("convert");
+}
+
+}  // namespace dfa

@@ -1,0 +1,336 @@
+// dfa_api.cu -- the C ABI (include/dfa.h): argument validation, workspace
+// layout, work-list upload, dispatch to the kernels and error reporting.
+// No exception crosses this boundary and no device memory is allocated here.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+#include <vector>
+
+#include "internal.h"
+
+namespace dfa {
+namespace {
+
+thread_local char g_msg[512] = "";
+std::atomic<int64_t> g_launches[DFA_KERNEL_KINDS];
+
+// Set by a kernel that gave up on a bounded wait; read by dfa_check_errors.
+__device__ int g_device_error;
+
+constexpr int kMaxDevices = 64;
+int* g_err_ptr[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+std::mutex g_mu;
+
+constexpr int kMaxWorkers = 1024;    // upper bound on the persistent grid
+constexpr int kFwdUnitRows = 256;    // query rows per forward work unit
+constexpr int kBwdUnitRows = 128;    // key rows per backward work unit
+
+size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int current_device() {
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return -1;
+    return d;
+}
+
+// Host-side cache of built work lists, kept in pinned memory so the upload is
+// a plain async copy (also legal inside stream capture).
+struct CachedList {
+    int32_t* host = nullptr;  // offsets[W+1] followed by items[n]
+    size_t count = 0;
+    int workers = 0;
+};
+std::map<std::tuple<int, int, int, int>, CachedList> g_lists;
+
+// Returns the pinned host copy of the list (nullptr on failure).
+const CachedList* get_list(int rows, int units, int workers, dfa_sched sched) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto key = std::make_tuple(rows, units, workers, (int)sched);
+    auto it = g_lists.find(key);
+    if (it != g_lists.end()) return &it->second;
+    const size_t n = (size_t)rows * units;
+    CachedList c;
+    c.count = (size_t)workers + 1 + n;
+    c.workers = workers;
+    if (cudaHostAlloc((void**)&c.host, c.count * sizeof(int32_t), cudaHostAllocDefault) != cudaSuccess)
+        return nullptr;
+    if (dfa_build_worklist(rows, units, workers, sched, c.host, c.host + workers + 1) < 0) {
+        cudaFreeHost(c.host);
+        return nullptr;
+    }
+    return &(g_lists[key] = c);
+}
+
+struct Layout {
+    size_t delta = 0, dq = 0, wl = 0, total = 0;
+};
+
+Layout layout(int B, int H, int Hkv, int S, int D, bool bwd) {
+    Layout L;
+    size_t off = 0;
+    if (bwd) {
+        L.delta = off;
+        off = align_up(off + sizeof(float) * (size_t)B * H * S);
+        L.dq = off;
+        off = align_up(off + sizeof(float) * (size_t)B * S * H * D);
+    }
+    L.wl = off;
+    const size_t units = bwd ? (size_t)(S + kBwdUnitRows - 1) / kBwdUnitRows
+                             : (size_t)(S + kFwdUnitRows - 1) / kFwdUnitRows;
+    const size_t rows = bwd ? (size_t)B * Hkv : (size_t)B * H;
+    off = align_up(off + sizeof(int32_t) * (kMaxWorkers + 1 + rows * units));
+    L.total = off;
+    return L;
+}
+
+dfa_status check_common(int B, int H, int Hkv, int D, float scale) {
+    if (B < 0 || H <= 0 || Hkv <= 0) return fail(DFA_ERR_INVALID_ARG, "B/H/H_kv must be >= 0/> 0/> 0");
+    if (H % Hkv != 0) return fail(DFA_ERR_INVALID_ARG, "H (%d) must be a multiple of H_kv (%d)", H, Hkv);
+    if (D != 64 && D != 128) return fail(DFA_ERR_UNSUPPORTED, "head dim D=%d (supported: 64, 128)", D);
+    if (!(scale > 0.f) || !std::isfinite(scale)) return fail(DFA_ERR_INVALID_ARG, "scale must be finite and > 0");
+    return DFA_OK;
+}
+
+dfa_status check_dtype(dfa_dtype dt) {
+    if (dt != DFA_F32 && dt != DFA_BF16) return fail(DFA_ERR_INVALID_ARG, "unknown dtype %d", (int)dt);
+    return DFA_OK;
+}
+
+dfa_status check_ptrs(std::initializer_list<const void*> ps) {
+    for (const void* p : ps) {
+        if (!p) return fail(DFA_ERR_INVALID_ARG, "null pointer");
+        if (!aligned16(p)) return fail(DFA_ERR_INVALID_ARG, "pointer %p is not 16-byte aligned", p);
+    }
+    return DFA_OK;
+}
+
+dfa_status upload_list(const CachedList* c, void* dst, cudaStream_t s) {
+    cudaError_t e = cudaMemcpyAsync(dst, c->host, c->count * sizeof(int32_t), cudaMemcpyHostToDevice, s);
+    return e == cudaSuccess ? DFA_OK : fail(DFA_ERR_CUDA, "work-list upload: %s", cudaGetErrorString(e));
+}
+
+}  // namespace
+
+dfa_status fail(dfa_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+void count_launch(dfa_kernel_kind kind, int n) { g_launches[kind].fetch_add(n); }
+
+int* device_error_flag() {
+    const int d = current_device();
+    if (d < 0) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_err_ptr[d]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+        g_err_ptr[d] = static_cast<int*>(p);
+    }
+    return g_err_ptr[d];
+}
+
+int num_sms() {
+    const int d = current_device();
+    if (d < 0) return 1;
+    if (!g_sms[d]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d);
+        g_sms[d] = n > 0 ? n : 1;
+    }
+    return g_sms[d];
+}
+
+}  // namespace dfa
+
+using namespace dfa;
+
+#ifndef DFA_TMP_SIMT_BWD
+#define DFA_TMP_SIMT_BWD 1
+#endif
+
+extern "C" const char* dfa_last_error(void) { return g_msg; }
+
+extern "C" int64_t dfa_launch_count(dfa_kernel_kind kind) {
+    if (kind < 0 || kind >= DFA_KERNEL_KINDS) return -1;
+    return g_launches[kind].load();
+}
+
+extern "C" size_t dfa_attn_workspace_size(int B, int H, int H_kv, int S, int D, int n_chunks, int bwd) {
+    if (B < 0 || H <= 0 || H_kv <= 0 || S < 0 || n_chunks <= 0 || (D != 64 && D != 128)) return 0;
+    if (H % H_kv != 0 || (S % n_chunks) != 0) return 0;
+    return layout(B, H, H_kv, S, D, bwd != 0).total;
+}
+
+extern "C" dfa_status dfa_chunk_attn_fwd(const void* q, const void* k, const void* v, dfa_dtype dt,
+                                         int B, int H, int H_kv, int Lq, int Lkv, int D,
+                                         const int64_t* q_strides, const int64_t* kv_strides,
+                                         int64_t q_offset, int64_t kv_offset, int causal, float scale,
+                                         float* O_partial, float* lse, void* stream) {
+    g_msg[0] = 0;
+    dfa_status st;
+    if ((st = check_dtype(dt)) || (st = check_common(B, H, H_kv, D, scale))) return st;
+    if (Lq < 0 || Lkv < 0) return fail(DFA_ERR_INVALID_ARG, "negative chunk length");
+    if (q_offset < 0 || kv_offset < 0) return fail(DFA_ERR_INVALID_ARG, "negative chunk offset");
+    if ((int64_t)B * Lq == 0) return DFA_OK;
+    if ((st = check_ptrs({q, O_partial, lse}))) return st;
+    if (Lkv > 0 && (st = check_ptrs({k, v}))) return st;
+    AttnProblem p{};
+    p.B = B; p.H = H; p.Hkv = H_kv; p.Lq = Lq; p.Lkv = Lkv; p.D = D;
+    p.q_sb = q_strides ? q_strides[0] : (int64_t)Lq * H * D;
+    p.q_ss = q_strides ? q_strides[1] : (int64_t)H * D;
+    p.q_sh = q_strides ? q_strides[2] : D;
+    p.kv_sb = kv_strides ? kv_strides[0] : (int64_t)Lkv * H_kv * D;
+    p.kv_ss = kv_strides ? kv_strides[1] : (int64_t)H_kv * D;
+    p.kv_sh = kv_strides ? kv_strides[2] : D;
+    for (int64_t x : {p.q_sb, p.q_ss, p.q_sh, p.kv_sb, p.kv_ss, p.kv_sh})
+        if (x < 0 || x % 8 != 0) return fail(DFA_ERR_INVALID_ARG, "strides must be non-negative multiples of 8 elements");
+    p.q_offset = q_offset; p.kv_offset = kv_offset; p.causal = causal != 0; p.scale = scale;
+    if (Lkv == 0) {
+        // No keys: every row is empty (O = 0, lse = -inf) -- handled by the kernels'
+        // empty-row path with an empty key loop.
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dt == DFA_F32) {
+        st = simt_fwd(p, dt, q, k, v, O_partial, true, lse, s);
+    } else {
+        st = tc_fwd(p, q, k, v, O_partial, true, lse, nullptr, s);
+    }
+    if (st == DFA_OK) count_launch(DFA_KERNEL_FWD);
+    return st;
+}
+
+extern "C" dfa_status dfa_merge_partials(int B, int H, int L, int D, const float* O_a, const float* lse_a,
+                                         const float* O_b, const float* lse_b, float* O_out, float* lse_out,
+                                         void* stream) {
+    g_msg[0] = 0;
+    if (B < 0 || H <= 0 || L < 0 || D <= 0 || D % 4 != 0)
+        return fail(DFA_ERR_INVALID_ARG, "bad merge sizes (B=%d H=%d L=%d D=%d)", B, H, L, D);
+    if ((int64_t)B * L == 0) return DFA_OK;
+    dfa_status st;
+    if ((st = check_ptrs({O_a, lse_a, O_b, lse_b, O_out, lse_out}))) return st;
+    st = launch_merge(B, H, L, D, O_a, lse_a, O_b, lse_b, O_out, lse_out, static_cast<cudaStream_t>(stream));
+    if (st == DFA_OK) count_launch(DFA_KERNEL_MERGE);
+    return st;
+}
+
+static dfa_status check_whole(dfa_dtype dt, int B, int H, int H_kv, int S, int D, int n_chunks,
+                              float scale, dfa_sched sched, void* workspace, size_t ws_bytes, bool bwd) {
+    dfa_status st;
+    if ((st = check_dtype(dt)) || (st = check_common(B, H, H_kv, D, scale))) return st;
+    if (S < 0) return fail(DFA_ERR_INVALID_ARG, "negative sequence length");
+    if (n_chunks <= 0 || S % n_chunks != 0)
+        return fail(DFA_ERR_INVALID_ARG, "S=%d must split into n_chunks=%d equal chunks", S, n_chunks);
+    if (sched != DFA_SCHED_BALANCED && sched != DFA_SCHED_UNBALANCED)
+        return fail(DFA_ERR_INVALID_ARG, "unknown schedule %d", (int)sched);
+    if ((int64_t)B * S == 0) return DFA_OK;
+    const size_t need = layout(B, H, H_kv, S, D, bwd).total;
+    if (!workspace || ws_bytes < need)
+        return fail(DFA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, ws_bytes);
+    if (!aligned16(workspace)) return fail(DFA_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
+    return DFA_OK;
+}
+
+static AttnProblem whole_problem(int B, int H, int H_kv, int S, int D, int causal, float scale) {
+    AttnProblem p{};
+    p.B = B; p.H = H; p.Hkv = H_kv; p.Lq = S; p.Lkv = S; p.D = D;
+    p.q_sb = (int64_t)S * H * D; p.q_ss = (int64_t)H * D; p.q_sh = D;
+    p.kv_sb = (int64_t)S * H_kv * D; p.kv_ss = (int64_t)H_kv * D; p.kv_sh = D;
+    p.q_offset = 0; p.kv_offset = 0; p.causal = causal != 0; p.scale = scale;
+    return p;
+}
+
+extern "C" dfa_status dfa_attn_fwd(const void* q, const void* k, const void* v, dfa_dtype dt, int B, int H,
+                                   int H_kv, int S, int D, int n_chunks, int causal, float scale,
+                                   dfa_sched sched, void* O, float* lse, void* workspace, size_t ws_bytes,
+                                   void* stream) {
+    g_msg[0] = 0;
+    dfa_status st = check_whole(dt, B, H, H_kv, S, D, n_chunks, scale, sched, workspace, ws_bytes, false);
+    if (st || (int64_t)B * S == 0) return st;
+    if ((st = check_ptrs({q, k, v, O, lse}))) return st;
+    const AttnProblem p = whole_problem(B, H, H_kv, S, D, causal, scale);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dt == DFA_F32) {
+        st = simt_fwd(p, dt, q, k, v, O, true, lse, s);
+    } else {
+        const Layout L = layout(B, H, H_kv, S, D, false);
+        const int units = (S + kFwdUnitRows - 1) / kFwdUnitRows;
+        const int workers = std::min(num_sms(), B * H * units);
+        const CachedList* c = get_list(B * H, units, workers, sched);
+        if (!c) return fail(DFA_ERR_CUDA, "could not build the work list");
+        int32_t* dev = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + L.wl);
+        if ((st = upload_list(c, dev, s))) return st;
+        WorkList wl{dev, dev + workers + 1, workers, units};
+        st = tc_fwd(p, q, k, v, O, false, lse, &wl, s);
+    }
+    if (st == DFA_OK) count_launch(DFA_KERNEL_FWD);
+    return st;
+}
+
+extern "C" dfa_status dfa_attn_bwd(const void* q, const void* k, const void* v, const void* O, const float* lse,
+                                   const void* dO, dfa_dtype dt, int B, int H, int H_kv, int S, int D,
+                                   int n_chunks, int causal, float scale, dfa_sched sched, void* dQ, void* dK,
+                                   void* dV, void* workspace, size_t ws_bytes, void* stream) {
+    g_msg[0] = 0;
+    dfa_status st = check_whole(dt, B, H, H_kv, S, D, n_chunks, scale, sched, workspace, ws_bytes, true);
+    if (st || (int64_t)B * S == 0) return st;
+    if ((st = check_ptrs({q, k, v, O, lse, dO, dQ, dK, dV}))) return st;
+    const AttnProblem p = whole_problem(B, H, H_kv, S, D, causal, scale);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const Layout L = layout(B, H, H_kv, S, D, true);
+    char* ws = static_cast<char*>(workspace);
+    float* delta = reinterpret_cast<float*>(ws + L.delta);
+    if ((st = launch_delta(dt, B, H, S, D, O, dO, delta, s))) return st;
+    count_launch(DFA_KERNEL_DELTA);
+    if (dt == DFA_F32 || DFA_TMP_SIMT_BWD) {
+        st = simt_bwd(p, dt, q, k, v, dO, lse, delta, dQ, dK, dV, s);
+        if (st == DFA_OK) count_launch(DFA_KERNEL_BWD, 2);
+        return st;
+    }
+    float* dq_acc = reinterpret_cast<float*>(ws + L.dq);
+    cudaError_t e = cudaMemsetAsync(dq_acc, 0, sizeof(float) * (size_t)B * S * H * D, s);
+    if (e != cudaSuccess) return fail(DFA_ERR_CUDA, "dQ accumulator clear: %s", cudaGetErrorString(e));
+    const int units = (S + kBwdUnitRows - 1) / kBwdUnitRows;
+    const int workers = std::min(num_sms(), B * H_kv * units);
+    const CachedList* c = get_list(B * H_kv, units, workers, sched);
+    if (!c) return fail(DFA_ERR_CUDA, "could not build the work list");
+    int32_t* dev = reinterpret_cast<int32_t*>(ws + L.wl);
+    if ((st = upload_list(c, dev, s))) return st;
+    WorkList wl{dev, dev + workers + 1, workers, units};
+    if ((st = tc_bwd(p, q, k, v, dO, lse, delta, dq_acc, dK, dV, &wl, s))) return st;
+    count_launch(DFA_KERNEL_BWD);
+    st = launch_convert(dt, (int64_t)B * S * H * D, scale, dq_acc, dQ, s);
+    if (st == DFA_OK) count_launch(DFA_KERNEL_CONVERT);
+    return st;
+}
+
+extern "C" dfa_status dfa_check_errors(void* stream) {
+    g_msg[0] = 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return fail(DFA_ERR_CUDA, "stream error: %s", cudaGetErrorString(e));
+    int* flag = device_error_flag();
+    if (!flag) return fail(DFA_ERR_CUDA, "device error flag unavailable");
+    int v = 0;
+    e = cudaMemcpy(&v, flag, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail(DFA_ERR_CUDA, "reading the error flag: %s", cudaGetErrorString(e));
+    if (v != 0) {
+        const int zero = 0;
+        cudaMemcpy(flag, &zero, sizeof(int), cudaMemcpyHostToDevice);
+        return fail(DFA_ERR_TIMEOUT, "a kernel gave up on a bounded wait (code %d)", v);
+    }
+    return DFA_OK;
+}

@@ -1,0 +1,67 @@
+// internal.h -- declarations shared by the library's translation units.
+// Not part of the public ABI (that is include/dfa.h).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/dfa.h"
+
+namespace dfa {
+
+// Problem description handed from the C ABI to the kernel launchers.
+// Element strides are for the (batch, seq, head) dimensions; D is contiguous.
+struct AttnProblem {
+    int B, H, Hkv, Lq, Lkv, D;
+    int64_t q_sb, q_ss, q_sh;     // Q (and dO when used) strides
+    int64_t kv_sb, kv_ss, kv_sh;  // K and V strides
+    int64_t q_offset, kv_offset;  // global token positions of row 0
+    int causal;
+    float scale;
+};
+
+// Device error flag (set by bounded waits that gave up).  Returns the device
+// address for the current device, or nullptr on failure.
+int* device_error_flag();
+
+// Records a message for dfa_last_error() and returns `st`.
+dfa_status fail(dfa_status st, const char* fmt, ...);
+
+// ---- fp32 CUDA-core kernels (simt_attn.cu) ----
+// Forward: O (dense [B,Lq,H,D], float or the input type) and lse (fp32 [B,H,Lq]).
+dfa_status simt_fwd(const AttnProblem& p, dfa_dtype dt, const void* q, const void* k,
+                    const void* v, void* O, bool O_is_f32, float* lse, cudaStream_t s);
+// Backward pieces: dQ (dense, dtype dt), dK/dV (dense, dtype dt).  Needs Delta.
+dfa_status simt_bwd(const AttnProblem& p, dfa_dtype dt, const void* q, const void* k,
+                    const void* v, const void* dO, const float* lse, const float* delta,
+                    void* dQ, void* dK, void* dV, cudaStream_t s);
+
+// ---- small HBM-bound kernels (aux_kernels.cu) ----
+dfa_status launch_merge(int B, int H, int L, int D, const float* Oa, const float* la,
+                        const float* Ob, const float* lb, float* O, float* l, cudaStream_t s);
+// Delta[b,h,i] = sum_d dO[b,i,h,d] * O[b,i,h,d]   (dense BSHD, fp32 out [B,H,S]).
+dfa_status launch_delta(dfa_dtype dt, int B, int H, int S, int D, const void* O,
+                        const void* dO, float* delta, cudaStream_t s);
+// out[x] = scale * acc[x] cast to dt, n elements.
+dfa_status launch_convert(dfa_dtype dt, int64_t n, float scale, const float* acc, void* out,
+                          cudaStream_t s);
+
+// ---- tcgen05 tensor-core kernels (fwd_tc.cu, bwd_tc.cu) ----
+struct WorkList {
+    const int32_t* offsets;  // [n_workers + 1], device
+    const int32_t* items;    // [n_items], device: row * n_units + unit
+    int n_workers;
+    int n_units;
+};
+dfa_status tc_fwd(const AttnProblem& p, const void* q, const void* k, const void* v, void* O,
+                  bool O_is_f32, float* lse, const WorkList* wl, cudaStream_t s);
+dfa_status tc_bwd(const AttnProblem& p, const void* q, const void* k, const void* v,
+                  const void* dO, const float* lse, const float* delta, float* dq_acc,
+                  void* dK, void* dV, const WorkList* wl, cudaStream_t s);
+
+int num_sms();
+
+// Host-side launch counters behind dfa_launch_count().
+void count_launch(dfa_kernel_kind kind, int n = 1);
+
+}  // namespace dfa

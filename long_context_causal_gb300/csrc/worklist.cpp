@@ -1,0 +1,104 @@
+// worklist.cpp -- host-side schedulers for the persistent attention kernels.
+//
+// DISTFLASHATTN (paperlayer.ai summary of arXiv 2310.03294), §3.2 and App. B:
+// under causal attention a worker that owns later tokens has more key/value
+// blocks to visit, so with one contiguous token range per worker roughly half
+// the workers sit idle; the balanced schedule lets the early workers take
+// over part of the late workers' work, which on one GPU becomes a work list
+// for persistent CTAs.  §4.5 quotes the resulting ideal speedups for eight
+// workers: 36 blocks in 8 steps (4.5x) unbalanced, in 5 steps (7.2x) balanced.
+#include <algorithm>
+#include <cstdint>
+#include <vector>
+
+#include "../../include/dfa.h"
+
+namespace {
+
+// Split n units into `parts` contiguous ranges; range r is [lo(r), lo(r+1)).
+inline int64_t range_lo(int64_t n, int64_t parts, int64_t r) { return (n * r) / parts; }
+
+}  // namespace
+
+extern "C" int64_t dfa_build_worklist(int n_rows, int n_units, int n_workers, dfa_sched sched,
+                                      int32_t* offsets, int32_t* items) {
+    if (n_rows < 0 || n_units < 0 || n_workers <= 0 || !offsets ||
+        (n_rows > 0 && n_units > 0 && !items))
+        return -1;
+    if (sched != DFA_SCHED_BALANCED && sched != DFA_SCHED_UNBALANCED) return -1;
+    if ((int64_t)n_rows * n_units > INT32_MAX) return -1;
+    const int64_t W = n_workers;
+    std::vector<std::vector<int32_t>> per(W);
+    std::vector<int64_t> cost(W, 0);
+    // Each worker walks the (batch, head) rows in the same order, so workers
+    // run on the same head at about the same time and share its K/V in L2.
+    if (sched == DFA_SCHED_UNBALANCED) {
+        // One contiguous range of units per worker, the same for every row.
+        for (int64_t row = 0; row < n_rows; ++row)
+            for (int64_t w = 0; w < W; ++w)
+                for (int64_t u = range_lo(n_units, W, w); u < range_lo(n_units, W, w + 1); ++u) {
+                    per[w].push_back((int32_t)(row * n_units + u));
+                    cost[w] += u + 1;
+                }
+    } else {
+        // Mirror pairs (n-1-u, u) cost n+1 tiles each; pairs are dealt to the
+        // workers cyclically across rows, so no worker holds more than one
+        // pair above the average.  The heavier unit of a pair goes first.
+        int64_t t = 0;
+        for (int64_t row = 0; row < n_rows; ++row)
+            for (int64_t u = 0; u < (n_units + 1) / 2; ++u, ++t) {
+                const int64_t w = t % W, heavy = n_units - 1 - u;
+                per[w].push_back((int32_t)(row * n_units + heavy));
+                cost[w] += heavy + 1;
+                if (heavy != u) {
+                    per[w].push_back((int32_t)(row * n_units + u));
+                    cost[w] += u + 1;
+                }
+            }
+    }
+    int64_t pos = 0, makespan = 0;
+    for (int64_t w = 0; w < W; ++w) {
+        offsets[w] = (int32_t)pos;
+        for (int32_t it : per[w]) items[pos++] = it;
+        makespan = std::max(makespan, cost[w]);
+    }
+    offsets[W] = (int32_t)pos;
+    return makespan;
+}
+
+extern "C" int dfa_chunk_schedule(int P, dfa_sched sched, int max_steps, int32_t* steps) {
+    if (P <= 0 || max_steps <= 0 || !steps) return -1;
+    if (sched != DFA_SCHED_BALANCED && sched != DFA_SCHED_UNBALANCED) return -1;
+    // Per worker, the ordered list of (qchunk, kvchunk) blocks it computes.
+    std::vector<std::vector<int32_t>> work(P);
+    auto block = [&](int qc, int kc) { return (int32_t)(qc * P + kc); };
+    if (sched == DFA_SCHED_UNBALANCED) {
+        for (int p = 0; p < P; ++p)
+            for (int t = 0; t <= p; ++t) work[p].push_back(block(p, t));
+    } else {
+        // Worker p >= P/2 owns p+1 blocks, its helper P-1-p owns P-p; together
+        // P+1, shared so both finish within ceil((P+1)/2) steps.  The helper
+        // computes its own blocks first, then the tail of the owner's blocks
+        // and hands the partial output and lse back for merging.
+        const int per_worker = (P + 2) / 2;   // ceil((P+1)/2)
+        for (int p = P - 1; p >= 0; --p) {
+            const int helper = P - 1 - p;
+            if (helper > p) break;             // pairs done
+            if (helper == p) {                 // odd P: the middle worker is alone
+                for (int t = 0; t <= p; ++t) work[p].push_back(block(p, t));
+                continue;
+            }
+            const int own = std::min(p + 1, per_worker);
+            for (int t = 0; t < own; ++t) work[p].push_back(block(p, t));
+            for (int t = 0; t <= helper; ++t) work[helper].push_back(block(helper, t));
+            for (int t = own; t <= p; ++t) work[helper].push_back(block(p, t));
+        }
+    }
+    int n_steps = 0;
+    for (auto& w : work) n_steps = std::max(n_steps, (int)w.size());
+    if (n_steps > max_steps) return -1;
+    for (int s = 0; s < n_steps; ++s)
+        for (int p = 0; p < P; ++p)
+            steps[s * P + p] = s < (int)work[p].size() ? work[p][s] : -1;
+    return n_steps;
+}

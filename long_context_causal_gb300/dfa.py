@@ -1,0 +1,219 @@
+"""Python binding of libdfa.so (include/dfa.h) -- argument marshalling only.
+
+Each function has the name of the C entry point it calls.  Torch tensors are
+used for device memory and streams: the binding reads their data pointers,
+sizes and strides, allocates missing outputs/workspace with torch, passes the
+current CUDA stream, and raises ``DfaError`` on any non-OK status.  All
+arithmetic runs in the library's CUDA kernels; there is no CPU fallback, and
+importing this module fails if the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdfa.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "dfa.h")
+
+DFA_OK, DFA_ERR_INVALID_ARG, DFA_ERR_UNSUPPORTED, DFA_ERR_CUDA, DFA_ERR_TIMEOUT, DFA_ERR_WORKSPACE = range(6)
+DFA_F32, DFA_BF16 = 0, 1
+DFA_SCHED_BALANCED, DFA_SCHED_UNBALANCED = 0, 1
+KERNEL_KINDS = {"fwd": 0, "bwd": 1, "merge": 2, "delta": 3, "convert": 4}
+_SCHED = {"balanced": DFA_SCHED_BALANCED, "unbalanced": DFA_SCHED_UNBALANCED,
+          DFA_SCHED_BALANCED: DFA_SCHED_BALANCED, DFA_SCHED_UNBALANCED: DFA_SCHED_UNBALANCED}
+
+
+class DfaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"dfa status {status}: {message}")
+        self.status = status
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built: run `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    p64 = ctypes.POINTER(ctypes.c_int64)
+    p32 = ctypes.POINTER(ctypes.c_int32)
+    sig = {
+        "dfa_chunk_attn_fwd": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, p64, p64, i64, i64, i32, f32, vp, vp, vp]),
+        "dfa_merge_partials": (i32, [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]),
+        "dfa_attn_workspace_size": (sz, [i32, i32, i32, i32, i32, i32, i32]),
+        "dfa_attn_fwd": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, f32, i32, vp, vp, vp, sz, vp]),
+        "dfa_attn_bwd": (i32, [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, f32, i32,
+                               vp, vp, vp, vp, sz, vp]),
+        "dfa_check_errors": (i32, [vp]),
+        "dfa_last_error": (ctypes.c_char_p, []),
+        "dfa_launch_count": (i64, [i32]),
+        "dfa_build_worklist": (i64, [i32, i32, i32, i32, p32, p32]),
+        "dfa_chunk_schedule": (i32, [i32, i32, i32, p32]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype, fn.argtypes = res, args
+    return lib
+
+
+_lib = _load()
+
+
+def header_functions() -> list[str]:
+    """Names of every function include/dfa.h declares."""
+    with open(HEADER) as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    return sorted(set(re.findall(r"\b(dfa_[a-z0-9_]+)\s*\(", text)))
+
+
+def library() -> ctypes.CDLL:
+    return _lib
+
+
+def _check(status: int):
+    if status != DFA_OK:
+        raise DfaError(status, _lib.dfa_last_error().decode())
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return DFA_F32
+    if t.dtype == torch.bfloat16:
+        return DFA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _ptr(t):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _dense(t: torch.Tensor, name: str):
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (BSHD dense)")
+
+
+# ---------------------------------------------------------------- entry points
+def dfa_chunk_attn_fwd(q, k, v, q_offset: int = 0, kv_offset: int = 0, causal: bool = True,
+                       scale: float | None = None, O_partial=None, lse=None, stream=None):
+    """One chunk step: returns (O_partial fp32 [B,Lq,H,D], lse fp32 [B,H,Lq])."""
+    B, Lq, H, D = q.shape
+    _, Lkv, Hkv, _ = k.shape
+    if k.stride() != v.stride() or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("k and v must share dtype and strides with each other (and dtype with q)")
+    if q.stride(3) != 1 or k.stride(3) != 1:
+        raise ValueError("the head dimension must be contiguous")
+    scale = D ** -0.5 if scale is None else float(scale)
+    if O_partial is None:
+        O_partial = torch.empty((B, Lq, H, D), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Lq), dtype=torch.float32, device=q.device)
+    qs = (ctypes.c_int64 * 3)(q.stride(0), q.stride(1), q.stride(2))
+    ks = (ctypes.c_int64 * 3)(k.stride(0), k.stride(1), k.stride(2))
+    _check(_lib.dfa_chunk_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _dtype(q), B, H, Hkv, Lq, Lkv, D,
+                                   qs, ks, int(q_offset), int(kv_offset), int(bool(causal)), scale,
+                                   _ptr(O_partial), _ptr(lse), _stream(stream)))
+    return O_partial, lse
+
+
+def dfa_merge_partials(O_a, lse_a, O_b, lse_b, O_out=None, lse_out=None, stream=None):
+    """Rescale-and-merge; O_out/lse_out may alias the inputs."""
+    B, L, H, D = O_a.shape
+    for t, n in ((O_a, "O_a"), (O_b, "O_b"), (lse_a, "lse_a"), (lse_b, "lse_b")):
+        _dense(t, n)
+    O_out = torch.empty_like(O_a) if O_out is None else O_out
+    lse_out = torch.empty_like(lse_a) if lse_out is None else lse_out
+    _check(_lib.dfa_merge_partials(B, H, L, D, _ptr(O_a), _ptr(lse_a), _ptr(O_b), _ptr(lse_b),
+                                   _ptr(O_out), _ptr(lse_out), _stream(stream)))
+    return O_out, lse_out
+
+
+def dfa_attn_workspace_size(B, H, H_kv, S, D, n_chunks, bwd) -> int:
+    return int(_lib.dfa_attn_workspace_size(B, H, H_kv, S, D, n_chunks, int(bool(bwd))))
+
+
+def workspace(B, H, H_kv, S, D, n_chunks, bwd, device="cuda"):
+    n = dfa_attn_workspace_size(B, H, H_kv, S, D, n_chunks, bwd)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+
+
+def dfa_attn_fwd(q, k, v, n_chunks: int = 1, causal: bool = True, scale: float | None = None,
+                 sched="balanced", O=None, lse=None, workspace_buf=None, stream=None):
+    """Whole-sequence forward: returns (O [B,S,H,D] in q's dtype, lse fp32 [B,H,S])."""
+    B, S, H, D = q.shape
+    Hkv = k.shape[2]
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _dense(t, n)
+    scale = D ** -0.5 if scale is None else float(scale)
+    O = torch.empty_like(q) if O is None else O
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device) if lse is None else lse
+    ws = workspace(B, H, Hkv, S, D, n_chunks, False, q.device) if workspace_buf is None else workspace_buf
+    _check(_lib.dfa_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _dtype(q), B, H, Hkv, S, D, int(n_chunks),
+                             int(bool(causal)), scale, _SCHED[sched], _ptr(O), _ptr(lse), _ptr(ws),
+                             ws.numel(), _stream(stream)))
+    return O, lse
+
+
+def dfa_attn_bwd(q, k, v, O, lse, dO, n_chunks: int = 1, causal: bool = True,
+                 scale: float | None = None, sched="balanced", dQ=None, dK=None, dV=None,
+                 workspace_buf=None, stream=None):
+    """Backward from the saved (O, lse): returns (dQ, dK, dV) in q's dtype."""
+    B, S, H, D = q.shape
+    Hkv = k.shape[2]
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (O, "O"), (lse, "lse"), (dO, "dO")):
+        _dense(t, n)
+    scale = D ** -0.5 if scale is None else float(scale)
+    dQ = torch.empty_like(q) if dQ is None else dQ
+    dK = torch.empty_like(k) if dK is None else dK
+    dV = torch.empty_like(v) if dV is None else dV
+    ws = workspace(B, H, Hkv, S, D, n_chunks, True, q.device) if workspace_buf is None else workspace_buf
+    _check(_lib.dfa_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(O), _ptr(lse), _ptr(dO), _dtype(q),
+                             B, H, Hkv, S, D, int(n_chunks), int(bool(causal)), scale, _SCHED[sched],
+                             _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(ws), ws.numel(), _stream(stream)))
+    return dQ, dK, dV
+
+
+def dfa_check_errors(stream=None):
+    _check(_lib.dfa_check_errors(_stream(stream)))
+
+
+def dfa_last_error() -> str:
+    return _lib.dfa_last_error().decode()
+
+
+def dfa_launch_count(kind: str | int) -> int:
+    return int(_lib.dfa_launch_count(KERNEL_KINDS.get(kind, kind)))
+
+
+def dfa_build_worklist(n_rows: int, n_units: int, n_workers: int, sched="balanced"):
+    """Host-only: returns (offsets list, items list, makespan in tiles)."""
+    import numpy as np
+    offsets = np.zeros(n_workers + 1, dtype=np.int32)
+    items = np.zeros(max(n_rows * n_units, 1), dtype=np.int32)
+    p32 = ctypes.POINTER(ctypes.c_int32)
+    mk = _lib.dfa_build_worklist(n_rows, n_units, n_workers, _SCHED[sched],
+                                 offsets.ctypes.data_as(p32), items.ctypes.data_as(p32))
+    if mk < 0:
+        raise DfaError(DFA_ERR_INVALID_ARG, "bad work-list arguments")
+    return offsets, items[: n_rows * n_units], int(mk)
+
+
+def dfa_chunk_schedule(P: int, sched="balanced"):
+    """Host-only: the per-step block schedule of P chunk workers -> int array [steps, P]."""
+    import numpy as np
+    cap = P + 1
+    steps = np.zeros(cap * P, dtype=np.int32)
+    n = _lib.dfa_chunk_schedule(P, _SCHED[sched], cap, steps.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)))
+    if n < 0:
+        raise DfaError(DFA_ERR_INVALID_ARG, "bad chunk-schedule arguments")
+    return steps[: n * P].reshape(n, P)

@@ -1,0 +1,84 @@
+"""Host-side schedulers (CPU only): coverage and makespan.
+
+DISTFLASHATTN §4.5 (Fig. 4) quotes the ideal speedups of its schedules for
+eight workers: 4.5x unbalanced and 7.2x balanced, i.e. 36 causal blocks
+finished in 8 and in 5 steps (App. B, Figs. 5-6).  The fixture
+tests/golden/balanced_schedule_fig4.json holds those printed numbers.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+from long_context_causal_gb300 import dfa
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def blocks_of(P):
+    return {qc * P + kc for qc in range(P) for kc in range(qc + 1)}
+
+
+@pytest.mark.parametrize("P", [1, 2, 3, 4, 5, 8, 16, 31, 32])
+@pytest.mark.parametrize("sched", ["balanced", "unbalanced"])
+def test_chunk_schedule_covers_every_causal_block_once(P, sched):
+    st = dfa.dfa_chunk_schedule(P, sched)
+    done = [int(b) for b in st.ravel() if b >= 0]
+    assert len(done) == len(set(done)) == P * (P + 1) // 2
+    assert set(done) == blocks_of(P)
+    expect = P if sched == "unbalanced" else (P + 2) // 2
+    assert st.shape[0] == expect
+
+
+def test_chunk_schedule_matches_the_pages_fig4_speedups():
+    with open(os.path.join(GOLDEN, "balanced_schedule_fig4.json")) as f:
+        fx = json.load(f)
+    P = fx["workers"]
+    total = P * (P + 1) // 2
+    unb = dfa.dfa_chunk_schedule(P, "unbalanced").shape[0]
+    bal = dfa.dfa_chunk_schedule(P, "balanced").shape[0]
+    assert total / unb == pytest.approx(fx["theoretical_speedup_unbalanced"])
+    assert total / bal == pytest.approx(fx["theoretical_speedup_balanced"])
+
+
+def test_balanced_helper_work_is_owned_by_a_mirror_worker():
+    P = 8
+    st = dfa.dfa_chunk_schedule(P, "balanced")
+    for s in range(st.shape[0]):
+        for w in range(P):
+            b = st[s, w]
+            if b < 0:
+                continue
+            qc = b // P
+            assert qc == w or qc == P - 1 - w     # own chunk or the mirrored owner's
+
+
+@pytest.mark.parametrize("rows,units,W", [(1, 4, 4), (32, 512, 148), (32, 1024, 152), (8, 512, 148),
+                                          (3, 7, 5), (2, 1, 8), (1, 300, 148)])
+@pytest.mark.parametrize("sched", ["balanced", "unbalanced"])
+def test_worklist_covers_every_unit_once(rows, units, W, sched):
+    off, items, mk = dfa.dfa_build_worklist(rows, units, W, sched)
+    assert off[0] == 0 and off[-1] == rows * units and np.all(np.diff(off) >= 0)
+    assert sorted(items.tolist()) == list(range(rows * units))
+    cost = [sum(int(i) % units + 1 for i in items[off[w]:off[w + 1]]) for w in range(W)]
+    assert mk == max(cost)
+    # Rows are walked in order by every worker (L2 sharing of one head's K/V).
+    for w in range(W):
+        r = items[off[w]:off[w + 1]] // units
+        assert np.all(np.diff(r) >= 0)
+
+
+def test_balanced_worklist_beats_unbalanced_makespan():
+    for rows, units, W in [(32, 512, 148), (32, 1024, 148), (8, 256, 148)]:
+        _, _, mb = dfa.dfa_build_worklist(rows, units, W, "balanced")
+        _, _, mu = dfa.dfa_build_worklist(rows, units, W, "unbalanced")
+        ideal = rows * units * (units + 1) / 2 / W
+        assert mb < mu
+        assert mb <= ideal + units + 1          # within one mirror pair of perfect
+        assert mu > 1.5 * ideal
+
+
+def test_worklist_rejects_bad_arguments():
+    with pytest.raises(dfa.DfaError):
+        dfa.dfa_build_worklist(1, 4, 0)
