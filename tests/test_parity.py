@@ -3,6 +3,8 @@
 Tolerances (max abs error unless stated):
   fp32 I/O:  O 1e-4, lse 1e-5, dQ/dK/dV 1e-3; chunked vs unchunked 1e-5
   bf16 I/O:  O 2e-2, lse 1e-3, each gradient 3e-2 x max|reference gradient|
+A gradient that is analytically zero (a single token: dS = P (dP - Delta) = 0)
+has no scale of its own; its relative error is taken against a floor of 1e-2.
 """
 import numpy as np
 import pytest
@@ -43,7 +45,7 @@ def check_grads(got, ref, dtype, what=""):
         if dtype == torch.float32:
             assert err <= tol["grad_abs"], f"{what}: {name} abs err {err}"
         else:
-            rel = err / max(np.max(np.abs(r)), 1e-30)
+            rel = err / max(np.max(np.abs(r)), 1e-2)
             assert rel <= tol["grad_rel"], f"{what}: {name} rel err {rel}"
 
 
