@@ -1,0 +1,499 @@
+// fwd_tc.cu -- tcgen05 tensor-core causal attention forward for sm_103a.
+//
+// DISTFLASHATTN (paperlayer.ai summary of arXiv 2310.03294): each query chunk
+// attends to the key/value chunks at or before it (§3.2), every chunk step
+// updates the attention state and yields an output with its log-sum-exp
+// (App. D), and states combine by the online-softmax rescale-and-merge rule.
+// Here one CTA owns a block of 256 query rows (two 128-row tiles) and streams
+// every visible 128-row key/value tile through shared memory; the running
+// (max, sum, unnormalised output) of each row IS the merged state of all
+// chunk steps so far, so partials of consecutive chunks merge on chip.
+//
+// Roles (384 threads, one CTA per SM, persistent over a host-built work list):
+//   warp 0      TMA producer: Q tiles once per block, then K_j, V_j into a
+//               ring of shared-memory slots (the single-GPU analogue of the
+//               pages' key/value prefetch overlapping compute, §3.2).
+//   warp 1      MMA issuer (one thread): S_w = Q_w K_j^T and O_w += P_w V_j
+//               on the 5th-generation tensor cores, fp32 accumulators in TMEM.
+//   warp 2      TMEM allocation.
+//   warps 4-11  two softmax warpgroups, one query row per thread: row max,
+//               exp2, row sum, P (bf16) written back into TMEM over S, lazy
+//               rescale of O, and the epilogue O/l, lse.
+// The two Q tiles ping-pong: while one warpgroup runs its softmax the tensor
+// cores run the other tile's MMAs.
+//
+// TMEM columns: S_0 [0,128) S_1 [128,256) O_0 [256,256+D) O_1 [384,384+D);
+// P_w (bf16 pairs) overwrites the first 64 columns of S_w.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dfa {
+namespace {
+
+using namespace ptx;
+
+constexpr int kThreads = 384;
+constexpr int BM = 128;            // query rows per tile (MMA M)
+constexpr int BN = 128;            // key rows per tile
+constexpr int kBlockRows = 2 * BM; // query rows per work unit
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;
+constexpr uint32_t kCtrlRegs = 56;
+constexpr uint32_t kSoftmaxRegs = 216;   // log2 units: rescale O only when the max grows by > 2^8
+
+template <int D>
+struct Cfg {
+    static constexpr int kTileBytes = BN * D * 2;              // one bf16 tile of 128 rows
+    static constexpr int kSlots = D == 128 ? 4 : 6;            // K/V ring depth
+    static constexpr int kQBytes = 2 * kTileBytes;
+    static constexpr int kSmem = kQBytes + kSlots * kTileBytes + 1024 /*barriers*/ + 1024 /*align*/;
+};
+
+struct FwdArgs {
+    int B, H, Hkv, Lq, Lkv;
+    int64_t q_offset, kv_offset;
+    int causal;
+    float scale_log2;      // scale * log2(e)
+    void* O;               // dense [B, Lq, H, D], bf16 or fp32
+    float* lse;            // [B, H, Lq]
+    const int32_t* wl_offsets;
+    const int32_t* wl_items;
+    int n_units;
+    int* err;
+};
+
+struct Item {
+    int b, h, g, q0, n_kv;
+};
+
+__device__ __forceinline__ Item decode(const FwdArgs& a, int it) {
+    Item x;
+    const int row = it / a.n_units, unit = it % a.n_units;
+    x.b = row / a.H;
+    x.h = row % a.H;
+    x.g = x.h / (a.H / a.Hkv);
+    x.q0 = unit * kBlockRows;
+    const int total = (a.Lkv + BN - 1) / BN;
+    if (!a.causal) {
+        x.n_kv = total;
+    } else {
+        const int64_t last_q = a.q_offset + min(x.q0 + kBlockRows, a.Lq) - 1;
+        const int64_t visible = last_q - a.kv_offset + 1;   // keys [0, visible) may be seen
+        const int64_t tiles = (visible + BN - 1) / BN;
+        x.n_kv = visible <= 0 ? 0 : (int)(tiles < total ? tiles : total);
+    }
+    return x;
+}
+
+template <int D, bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 1)
+fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+              const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sQ = smem;                                   // 2 tiles
+    uint8_t* sKV = smem + C::kQBytes;                     // ring
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + C::kSlots * C::kTileBytes);
+    uint64_t* q_full = bars + 0;
+    uint64_t* q_empty = bars + 1;
+    uint64_t* s_full = bars + 2;          // [2]
+    uint64_t* p_full = bars + 4;          // [2]
+    uint64_t* o_full = bars + 6;          // [2]
+    uint64_t* done = bars + 8;
+    uint64_t* kv_full = bars + 16;        // [kSlots]
+    uint64_t* kv_empty = bars + 16 + C::kSlots;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 32);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 33);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    int it_begin, it_end;
+    if (a.wl_items) {
+        it_begin = a.wl_offsets[blockIdx.x];
+        it_end = a.wl_offsets[blockIdx.x + 1];
+    } else {
+        it_begin = blockIdx.x;
+        it_end = blockIdx.x + 1;
+    }
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
+        for (int w = 0; w < 2; ++w) {
+            mbar_init(&s_full[w], 1);
+            mbar_init(&p_full[w], BM);
+            mbar_init(&o_full[w], 1);
+        }
+        mbar_init(done, 1);
+        for (int s = 0; s < C::kSlots; ++s) {
+            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    if (warp == 2) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        uint32_t ld = 0, qi = 0, qi_issued = 0;
+        bool ok = true;
+        for (int it = it_begin; it < it_end && ok; ++it) {
+            const Item x = decode(a, it);
+            if (x.n_kv == 0) continue;
+            ok = __all_sync(0xffffffffu, mbar_wait(q_empty, (qi & 1) ^ 1, abort_flag, a.err));
+            if (!ok) break;
+            ++qi_issued;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(q_full, C::kQBytes);
+                for (int w = 0; w < 2; ++w)
+                    for (int blk = 0; blk < D / 64; ++blk)
+                        tma_load_4d(sQ + w * C::kTileBytes + blk * 16384, &tmQ, q_full, blk * 64, x.h,
+                                    x.q0 + w * BM, x.b);
+            }
+            __syncwarp();
+            for (int j = 0; j < x.n_kv && ok; ++j) {
+                for (int which = 0; which < 2; ++which, ++ld) {
+                    const int slot = ld % C::kSlots;
+                    ok = __all_sync(0xffffffffu, mbar_wait(&kv_empty[slot], ((ld / C::kSlots) & 1) ^ 1,
+                                                           abort_flag, a.err));
+                    if (!ok) break;
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&kv_full[slot], C::kTileBytes);
+                        for (int blk = 0; blk < D / 64; ++blk)
+                            tma_load_4d(sKV + slot * C::kTileBytes + blk * 16384, which ? &tmV : &tmK,
+                                        &kv_full[slot], blk * 64, x.g, j * BN, x.b);
+                    }
+                    __syncwarp();
+                }
+            }
+            ++qi;
+        }
+        if (!ok && lane == 0) {
+            // Aborted: let the copies already issued land before the CTA exits.
+            // The newest load into each used slot is the only one possibly in flight.
+            int dummy = 0;
+            for (uint32_t s = 0; s < (uint32_t)C::kSlots && s < ld; ++s) {
+                const uint32_t last = s + C::kSlots * ((ld - 1 - s) / C::kSlots);
+                mbar_wait(&kv_full[s], (last / C::kSlots) & 1, &dummy, nullptr);
+            }
+            if (qi_issued > 0) mbar_wait(q_full, (qi_issued - 1) & 1, &dummy, nullptr);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        const uint32_t idS = idesc_bf16_f32(BM, BN, false, false);
+        const uint32_t idO = idesc_bf16_f32(BM, D, false, true);
+        const uint32_t qaddr = smem_u32(sQ), kvaddr = smem_u32(sKV);
+        uint32_t cons = 0, t = 0, qi = 0;
+        bool ok = true;
+        auto issue_S = [&](int w, uint32_t slot) {
+            if (lane == 0) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+                    mma_ss(tmem + w * 128, sdesc_sw128(qaddr + w * C::kTileBytes + off, 16, 1024),
+                           sdesc_sw128(kvaddr + slot * C::kTileBytes + off, 16, 1024), idS, kk > 0);
+                }
+            }
+        };
+        auto issue_PV = [&](int w, uint32_t slot, bool acc) {
+            if (lane == 0) {
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    mma_ts(tmem + 256 + w * 128, tmem + w * 128 + kk * 8,
+                           sdesc_sw128(kvaddr + slot * C::kTileBytes + kk * 2048, 16384, 1024), idO,
+                           (acc || kk > 0) ? 1u : 0u);
+                }
+            }
+        };
+        auto wait = [&](uint64_t* bar, uint32_t parity) {
+            ok = ok && __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, a.err));
+            if (ok) tc_fence_after();
+            return ok;
+        };
+        auto commit = [&](uint64_t* bar) {
+            if (lane == 0) mma_commit(bar);
+            __syncwarp();
+        };
+        for (int it = it_begin; it < it_end && ok; ++it) {
+            const Item x = decode(a, it);
+            if (x.n_kv == 0) continue;
+            if (!wait(q_full, qi & 1)) break;
+            uint32_t slotK = cons % C::kSlots;
+            if (!wait(&kv_full[slotK], (cons / C::kSlots) & 1)) break;
+            issue_S(0, slotK);
+            commit(&s_full[0]);
+            issue_S(1, slotK);
+            commit(&s_full[1]);
+            commit(&kv_empty[slotK]);
+            ++cons;
+            for (int j = 0; j < x.n_kv && ok; ++j, ++t) {
+                const bool more = j + 1 < x.n_kv;
+                const uint32_t slotV = cons % C::kSlots;
+                if (!wait(&kv_full[slotV], (cons / C::kSlots) & 1)) break;
+                if (!wait(&p_full[0], t & 1)) break;
+                issue_PV(0, slotV, j > 0);
+                if (!more) commit(&o_full[0]);
+                uint32_t slotK1 = (cons + 1) % C::kSlots;
+                if (more) {
+                    if (!wait(&kv_full[slotK1], ((cons + 1) / C::kSlots) & 1)) break;
+                    issue_S(0, slotK1);
+                    commit(&s_full[0]);
+                }
+                if (!wait(&p_full[1], t & 1)) break;
+                issue_PV(1, slotV, j > 0);
+                commit(&kv_empty[slotV]);
+                if (!more) commit(&o_full[1]);
+                if (more) {
+                    issue_S(1, slotK1);
+                    commit(&s_full[1]);
+                    commit(&kv_empty[slotK1]);
+                }
+                cons += more ? 2 : 1;
+            }
+            if (!ok) break;
+            commit(q_empty);
+            ++qi;
+        }
+        // Drain: every MMA this thread issued has finished before TMEM is freed.
+        commit(done);
+        int dummy = 0;
+        mbar_wait(done, 0, &dummy, a.err);
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ softmax warpgroups
+        const int w = (warp - 4) / 4;                 // which query tile
+        const int r = (warp % 4) * 32 + lane;         // row within the tile == TMEM lane
+        const uint32_t lane_base = (uint32_t)((warp % 4) * 32) << 16;
+        const uint32_t tS = tmem + lane_base + w * 128;
+        const uint32_t tO = tmem + lane_base + 256 + w * 128;
+        const float c2 = a.scale_log2;
+        uint32_t t = 0, qi = 0;
+        bool ok = true;
+        for (int it = it_begin; it < it_end && ok; ++it) {
+            const Item x = decode(a, it);
+            const int row = x.q0 + w * BM + r;                 // row within the query chunk
+            const int64_t qpos = a.q_offset + row;
+            float m_run = -INFINITY, l = 0.f;
+            for (int j = 0; j < x.n_kv; ++j, ++t) {
+                ok = __all_sync(0xffffffffu, mbar_wait(&s_full[w], t & 1, abort_flag, a.err));
+                if (!ok) break;
+                tc_fence_after();
+                // Pass 1: row max over the tile (S read from TMEM 32 columns at a time).
+                const int kv0 = j * BN;
+                const bool edge = kv0 + BN > a.Lkv;
+                const bool diag = a.causal && (a.kv_offset + kv0 + BN - 1 > a.q_offset + x.q0 + w * BM);
+                const bool masked = edge || diag;
+                // Column c of this tile is visible iff c < lim (both conditions are prefix limits).
+                int lim = BN;
+                if (masked) {
+                    int64_t v = (int64_t)a.Lkv - kv0;
+                    if (a.causal) {
+                        const int64_t vc = qpos - a.kv_offset - kv0 + 1;
+                        v = vc < v ? vc : v;
+                    }
+                    lim = v < 0 ? 0 : (v > BN ? BN : (int)v);
+                }
+                float mx = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t u[32];
+                    tmem_ld32(tS + c * 32, u);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        mx = fmaxf(mx, (c * 32 + e < lim) ? __uint_as_float(u[e]) : -INFINITY);
+                }
+                const float mx2 = mx * c2;
+                if (mx2 > m_run + kRescaleThreshold) {
+                    if (m_run != -INFINITY) {
+                        const float alpha = ex2(m_run - mx2);
+                        l *= alpha;
+                        if (j > 0) {
+#pragma unroll 1
+                            for (int c = 0; c < D / 32; ++c) {
+                                uint32_t u[32];
+                                tmem_ld32(tO + c * 32, u);
+#pragma unroll
+                                for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
+                                tmem_st32(tO + c * 32, u);
+                            }
+                        }
+                    }
+                    m_run = mx2;
+                }
+                const float m_use = m_run == -INFINITY ? 0.f : m_run;
+                // Pass 2: P = exp2(s * c2 - m), row sum, bf16 P written over S.
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t u[32];
+                    tmem_ld32(tS + c * 32, u);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int c0 = c * 32 + 2 * e;
+                        const float p0 = c0 < lim ? ex2(fmaf(__uint_as_float(u[2 * e]), c2, -m_use)) : 0.f;
+                        const float p1 = c0 + 1 < lim ? ex2(fmaf(__uint_as_float(u[2 * e + 1]), c2, -m_use)) : 0.f;
+                        l += p0 + p1;
+                        pk[e] = pack_bf16(p0, p1);
+                    }
+                    tmem_st16(tS + c * 16, pk);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&p_full[w]);
+            }
+            if (!ok) break;
+            // ---- epilogue: O = O_acc / l, lse = ln(sum exp(s))
+            const bool valid_row = row < a.Lq;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const int64_t orow = (((int64_t)x.b * a.Lq + row) * a.H + x.h) * D;
+            if (x.n_kv > 0) {
+                ok = __all_sync(0xffffffffu, mbar_wait(&o_full[w], qi & 1, abort_flag, a.err));
+                if (!ok) break;
+                tc_fence_after();
+                ++qi;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t u[32];
+                    tmem_ld32(tO + c * 32, u);
+                    if (valid_row) {
+                        if (OUT_F32) {
+                            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.O) + orow + c * 32);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                dst[e] = make_float4(__uint_as_float(u[4 * e]) * inv, __uint_as_float(u[4 * e + 1]) * inv,
+                                                     __uint_as_float(u[4 * e + 2]) * inv,
+                                                     __uint_as_float(u[4 * e + 3]) * inv);
+                        } else {
+                            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.O) + orow + c * 32);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                uint4 v;
+                                v.x = pack_bf16(__uint_as_float(u[8 * e + 0]) * inv, __uint_as_float(u[8 * e + 1]) * inv);
+                                v.y = pack_bf16(__uint_as_float(u[8 * e + 2]) * inv, __uint_as_float(u[8 * e + 3]) * inv);
+                                v.z = pack_bf16(__uint_as_float(u[8 * e + 4]) * inv, __uint_as_float(u[8 * e + 5]) * inv);
+                                v.w = pack_bf16(__uint_as_float(u[8 * e + 6]) * inv, __uint_as_float(u[8 * e + 7]) * inv);
+                                dst[e] = v;
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+            } else if (valid_row) {
+                for (int c = 0; c < D; ++c) {
+                    if (OUT_F32) static_cast<float*>(a.O)[orow + c] = 0.f;
+                    else static_cast<__nv_bfloat16*>(a.O)[orow + c] = __float2bfloat16_rn(0.f);
+                }
+            }
+            if (valid_row)
+                a.lse[((int64_t)x.b * a.H + x.h) * a.Lq + row] = l > 0.f ? (m_run + __log2f(l)) * kLn2 : -INFINITY;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 2) tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+}  // namespace
+
+// 4-D bf16 tensor map over [B, L, heads, D] (element strides sb, ss, sh; D
+// contiguous) with a {64, 1, 128, 1} box and the 128-byte swizzle.
+bool make_tmap_bshd(void* map, const void* base, int B, int L, int heads, int D, int64_t sb,
+                    int64_t ss, int64_t sh) {
+    CUtensorMap* m = static_cast<CUtensorMap*>(map);
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)(L > 0 ? L : 1), (cuuint64_t)(B > 0 ? B : 1)};
+    cuuint64_t strides[3] = {(cuuint64_t)sh * 2, (cuuint64_t)ss * 2, (cuuint64_t)sb * 2};
+    cuuint32_t box[4] = {64, 1, 128, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    // A stride of a size-1 dimension is never used; keep it valid for the encoder.
+    if (heads == 1 && strides[0] == 0) strides[0] = 16;
+    if (strides[0] == 0) strides[0] = 16;
+    if (strides[1] == 0) strides[1] = 16;
+    if (strides[2] == 0) strides[2] = 16;
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int D, bool OUT_F32>
+static dfa_status launch(const AttnProblem& p, const void* q, const void* k, const void* v, void* O,
+                         float* lse, const WorkList* wl, cudaStream_t s) {
+    CUtensorMap mq, mk, mv;
+    // With no keys nothing is loaded from K/V; any valid address serves the encoder.
+    if (p.Lkv == 0) k = v = q;
+    if (!make_tmap_bshd(&mq, q, p.B, p.Lq, p.H, D, p.q_sb, p.q_ss, p.q_sh) ||
+        !make_tmap_bshd(&mk, k, p.B, p.Lkv, p.Hkv, D, p.kv_sb, p.kv_ss, p.kv_sh) ||
+        !make_tmap_bshd(&mv, v, p.B, p.Lkv, p.Hkv, D, p.kv_sb, p.kv_ss, p.kv_sh))
+        return fail(DFA_ERR_CUDA, "tensor map encoding failed");
+    FwdArgs a{};
+    a.B = p.B; a.H = p.H; a.Hkv = p.Hkv; a.Lq = p.Lq; a.Lkv = p.Lkv;
+    a.q_offset = p.q_offset; a.kv_offset = p.kv_offset; a.causal = p.causal;
+    a.scale_log2 = p.scale * kLog2e;
+    a.O = O; a.lse = lse;
+    a.n_units = (p.Lq + kBlockRows - 1) / kBlockRows;
+    a.err = device_error_flag();
+    int grid;
+    if (wl) {
+        a.wl_offsets = wl->offsets;
+        a.wl_items = wl->items;
+        grid = wl->n_workers;
+    } else {
+        a.wl_offsets = nullptr;
+        a.wl_items = nullptr;
+        grid = p.B * p.H * a.n_units;
+    }
+    auto kern = fwd_tc_kernel<D, OUT_F32>;
+    const int smem = Cfg<D>::kSmem;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return fail(DFA_ERR_CUDA, "fwd_tc: shared memory attribute");
+    if (grid <= 0) return DFA_OK;
+    kern<<<grid, kThreads, smem, s>>>(mq, mk, mv, a);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? DFA_OK : fail(DFA_ERR_CUDA, "fwd_tc launch: %s", cudaGetErrorString(e));
+}
+
+dfa_status tc_fwd(const AttnProblem& p, const void* q, const void* k, const void* v, void* O,
+                  bool O_is_f32, float* lse, const WorkList* wl, cudaStream_t s) {
+    if (p.B == 0 || p.Lq == 0) return DFA_OK;
+    if (p.D == 128) return O_is_f32 ? launch<128, true>(p, q, k, v, O, lse, wl, s) : launch<128, false>(p, q, k, v, O, lse, wl, s);
+    return O_is_f32 ? launch<64, true>(p, q, k, v, O, lse, wl, s) : launch<64, false>(p, q, k, v, O, lse, wl, s);
+}
+
+}  // namespace dfa

@@ -61,6 +61,12 @@ dfa_status tc_bwd(const AttnProblem& p, const void* q, const void* k, const void
 
 int num_sms();
 
+// 4-D bf16 TMA descriptor over a [B, L, heads, D] tensor (element strides sb,
+// ss, sh; D contiguous), box {64, 1, 128, 1}, 128-byte swizzle.  The map is
+// written into `map` (a CUtensorMap, 128 bytes, 64-byte aligned).
+bool make_tmap_bshd(void* map, const void* base, int B, int L, int heads, int D, int64_t sb,
+                    int64_t ss, int64_t sh);
+
 // Host-side launch counters behind dfa_launch_count().
 void count_launch(dfa_kernel_kind kind, int n = 1);
 

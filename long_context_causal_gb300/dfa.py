@@ -17,7 +17,8 @@ import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libdfa.so")
-HEADER = os.path.join(os.path.dirname(_PKG), "include", "dfa.h")
+INCLUDE = os.path.join(os.path.dirname(_PKG), "include")
+HEADER = os.path.join(INCLUDE, "dfa.h")
 
 DFA_OK, DFA_ERR_INVALID_ARG, DFA_ERR_UNSUPPORTED, DFA_ERR_CUDA, DFA_ERR_TIMEOUT, DFA_ERR_WORKSPACE = range(6)
 DFA_F32, DFA_BF16 = 0, 1
@@ -52,6 +53,7 @@ def _load() -> ctypes.CDLL:
         "dfa_launch_count": (i64, [i32]),
         "dfa_build_worklist": (i64, [i32, i32, i32, i32, p32, p32]),
         "dfa_chunk_schedule": (i32, [i32, i32, i32, p32]),
+        "dfa_debug_mma": (i32, [i32, vp, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -63,10 +65,14 @@ _lib = _load()
 
 
 def header_functions() -> list[str]:
-    """Names of every function include/dfa.h declares."""
-    with open(HEADER) as f:
-        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
-    return sorted(set(re.findall(r"\b(dfa_[a-z0-9_]+)\s*\(", text)))
+    """Names of every function the headers under include/ declare."""
+    names = set()
+    for h in sorted(os.listdir(INCLUDE)):
+        if h.endswith(".h"):
+            with open(os.path.join(INCLUDE, h)) as f:
+                text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+            names.update(re.findall(r"\b(dfa_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
 
 
 def library() -> ctypes.CDLL:
@@ -181,6 +187,13 @@ def dfa_attn_bwd(q, k, v, O, lse, dO, n_chunks: int = 1, causal: bool = True,
                              B, H, Hkv, S, D, int(n_chunks), int(bool(causal)), scale, _SCHED[sched],
                              _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(ws), ws.numel(), _stream(stream)))
     return dQ, dK, dV
+
+
+def dfa_debug_mma(form: int, A, B, C=None, stream=None):
+    """One 128x128x128 tcgen05 product of the given operand form (include/dfa_debug.h)."""
+    C = torch.empty((128, 128), dtype=torch.float32, device=A.device) if C is None else C
+    _check(_lib.dfa_debug_mma(int(form), _ptr(A), _ptr(B), _ptr(C), _stream(stream)))
+    return C
 
 
 def dfa_check_errors(stream=None):
