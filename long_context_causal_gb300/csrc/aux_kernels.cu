@@ -98,6 +98,41 @@ delta_kernel(int B, int H, int S, int D, const T* __restrict__ O, const T* __res
     }
 }
 
+// One warp per (b, i, h) row of the padded range i < S_pad.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+bwd_prep_kernel(int B, int H, int S, int S_pad, int D, const T* __restrict__ O, const T* __restrict__ dO,
+                const float* __restrict__ lse, float* __restrict__ lse2, float* __restrict__ delta) {
+    const int64_t row = (int64_t)blockIdx.x * (kThreads / 32) + threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    if (row >= (int64_t)B * S_pad * H) return;
+    const int h = row % H;
+    const int64_t bi = row / H;
+    const int i = bi % S_pad, b = bi / S_pad;
+    const int64_t dst = ((int64_t)b * H + h) * S_pad + i;
+    if (i >= S) {
+        if (lane == 0) {
+            lse2[dst] = 0.f;
+            delta[dst] = 0.f;
+        }
+        return;
+    }
+    const int64_t src = (((int64_t)b * S + i) * H + h) * D;
+    float acc = 0.f;
+    for (int x = lane; x < D / 8; x += 32) {
+        float a[8], c[8];
+        load8<T>(O + src + 8 * x, a);
+        load8<T>(dO + src + 8 * x, c);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc = fmaf(a[e], c[e], acc);
+    }
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) {
+        delta[dst] = acc;
+        lse2[dst] = lse[((int64_t)b * H + h) * S + i] * 1.4426950408889634f;
+    }
+}
+
 __global__ void convert_bf16_kernel(int64_t n, float scale, const float* __restrict__ in,
                                     __nv_bfloat16* __restrict__ out) {
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -147,6 +182,20 @@ dfa_status launch_delta(dfa_dtype dt, int B, int H, int S, int D, const void* O,
         delta_kernel<__nv_bfloat16><<<(unsigned)blocks, kThreads, 0, s>>>(
             B, H, S, D, (const __nv_bfloat16*)O, (const __nv_bfloat16*)dO, delta);
     return launched("delta");
+}
+
+dfa_status launch_bwd_prep(dfa_dtype dt, int B, int H, int S, int S_pad, int D, const void* O,
+                           const void* dO, const float* lse, float* lse2, float* delta, cudaStream_t s) {
+    const int64_t rows = (int64_t)B * S_pad * H;
+    if (rows == 0) return DFA_OK;
+    const int64_t blocks = (rows + kThreads / 32 - 1) / (kThreads / 32);
+    if (dt == DFA_F32)
+        bwd_prep_kernel<float><<<(unsigned)blocks, kThreads, 0, s>>>(B, H, S, S_pad, D, (const float*)O,
+                                                                     (const float*)dO, lse, lse2, delta);
+    else
+        bwd_prep_kernel<__nv_bfloat16><<<(unsigned)blocks, kThreads, 0, s>>>(
+            B, H, S, S_pad, D, (const __nv_bfloat16*)O, (const __nv_bfloat16*)dO, lse, lse2, delta);
+    return launched("bwd prep");
 }
 
 dfa_status launch_convert(dfa_dtype dt, int64_t n, float scale, const float* acc, void* out,

@@ -72,15 +72,19 @@ const CachedList* get_list(int rows, int units, int workers, dfa_sched sched) {
 }
 
 struct Layout {
-    size_t delta = 0, dq = 0, wl = 0, total = 0;
+    size_t delta = 0, lse2 = 0, dq = 0, wl = 0, total = 0;
+    int S_pad = 0;
 };
 
 Layout layout(int B, int H, int Hkv, int S, int D, bool bwd) {
     Layout L;
     size_t off = 0;
+    L.S_pad = (S + kBwdUnitRows - 1) / kBwdUnitRows * kBwdUnitRows;
     if (bwd) {
         L.delta = off;
-        off = align_up(off + sizeof(float) * (size_t)B * H * S);
+        off = align_up(off + sizeof(float) * (size_t)B * H * L.S_pad);
+        L.lse2 = off;
+        off = align_up(off + sizeof(float) * (size_t)B * H * L.S_pad);
         L.dq = off;
         off = align_up(off + sizeof(float) * (size_t)B * S * H * D);
     }
@@ -158,9 +162,6 @@ int num_sms() {
 
 using namespace dfa;
 
-#ifndef DFA_TMP_SIMT_BWD
-#define DFA_TMP_SIMT_BWD 1
-#endif
 
 extern "C" const char* dfa_last_error(void) { return g_msg; }
 
@@ -293,13 +294,16 @@ extern "C" dfa_status dfa_attn_bwd(const void* q, const void* k, const void* v, 
     const Layout L = layout(B, H, H_kv, S, D, true);
     char* ws = static_cast<char*>(workspace);
     float* delta = reinterpret_cast<float*>(ws + L.delta);
-    if ((st = launch_delta(dt, B, H, S, D, O, dO, delta, s))) return st;
-    count_launch(DFA_KERNEL_DELTA);
-    if (dt == DFA_F32 || DFA_TMP_SIMT_BWD) {
+    if (dt == DFA_F32) {
+        if ((st = launch_delta(dt, B, H, S, D, O, dO, delta, s))) return st;
+        count_launch(DFA_KERNEL_DELTA);
         st = simt_bwd(p, dt, q, k, v, dO, lse, delta, dQ, dK, dV, s);
         if (st == DFA_OK) count_launch(DFA_KERNEL_BWD, 2);
         return st;
     }
+    float* lse2 = reinterpret_cast<float*>(ws + L.lse2);
+    if ((st = launch_bwd_prep(dt, B, H, S, L.S_pad, D, O, dO, lse, lse2, delta, s))) return st;
+    count_launch(DFA_KERNEL_DELTA);
     float* dq_acc = reinterpret_cast<float*>(ws + L.dq);
     cudaError_t e = cudaMemsetAsync(dq_acc, 0, sizeof(float) * (size_t)B * S * H * D, s);
     if (e != cudaSuccess) return fail(DFA_ERR_CUDA, "dQ accumulator clear: %s", cudaGetErrorString(e));
@@ -310,7 +314,7 @@ extern "C" dfa_status dfa_attn_bwd(const void* q, const void* k, const void* v, 
     int32_t* dev = reinterpret_cast<int32_t*>(ws + L.wl);
     if ((st = upload_list(c, dev, s))) return st;
     WorkList wl{dev, dev + workers + 1, workers, units};
-    if ((st = tc_bwd(p, q, k, v, dO, lse, delta, dq_acc, dK, dV, &wl, s))) return st;
+    if ((st = tc_bwd(p, q, k, v, dO, lse2, delta, L.S_pad, dq_acc, dK, dV, &wl, s))) return st;
     count_launch(DFA_KERNEL_BWD);
     st = launch_convert(dt, (int64_t)B * S * H * D, scale, dq_acc, dQ, s);
     if (st == DFA_OK) count_launch(DFA_KERNEL_CONVERT);

@@ -46,9 +46,7 @@ constexpr int BN = 128;            // key rows per tile
 constexpr int kBlockRows = 2 * BM; // query rows per work unit
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f;
-constexpr uint32_t kCtrlRegs = 56;
-constexpr uint32_t kSoftmaxRegs = 216;   // log2 units: rescale O only when the max grows by > 2^8
+constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O only when the max grows by > 2^8
 
 template <int D>
 struct Cfg {
@@ -322,22 +320,29 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                         mx = fmaxf(mx, (c * 32 + e < lim) ? __uint_as_float(u[e]) : -INFINITY);
                 }
                 const float mx2 = mx * c2;
+                // Lazy rescale: move this row's reference max only when the tile
+                // max exceeds it by more than 2^8.  The decision is per row, but
+                // tcgen05.ld/st are warp-collective, so the O rescale runs for the
+                // whole warp whenever any of its rows needs it (alpha = 1 elsewhere).
+                float alpha = 1.f;
+                bool resc = false;
                 if (mx2 > m_run + kRescaleThreshold) {
                     if (m_run != -INFINITY) {
-                        const float alpha = ex2(m_run - mx2);
+                        alpha = ex2(m_run - mx2);
                         l *= alpha;
-                        if (j > 0) {
-#pragma unroll 1
-                            for (int c = 0; c < D / 32; ++c) {
-                                uint32_t u[32];
-                                tmem_ld32(tO + c * 32, u);
-#pragma unroll
-                                for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
-                                tmem_st32(tO + c * 32, u);
-                            }
-                        }
+                        resc = true;
                     }
                     m_run = mx2;
+                }
+                if (j > 0 && __any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t u[32];
+                        tmem_ld32(tO + c * 32, u);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
+                        tmem_st32(tO + c * 32, u);
+                    }
                 }
                 const float m_use = m_run == -INFINITY ? 0.f : m_run;
                 // Pass 2: P = exp2(s * c2 - m), row sum, bf16 P written over S.

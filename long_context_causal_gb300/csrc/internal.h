@@ -42,6 +42,10 @@ dfa_status launch_merge(int B, int H, int L, int D, const float* Oa, const float
 // Delta[b,h,i] = sum_d dO[b,i,h,d] * O[b,i,h,d]   (dense BSHD, fp32 out [B,H,S]).
 dfa_status launch_delta(dfa_dtype dt, int B, int H, int S, int D, const void* O,
                         const void* dO, float* delta, cudaStream_t s);
+// Backward preprocessing for the tensor-core path: lse2 = lse * log2(e) and
+// Delta = rowsum(dO * O), both written to [B, H, S_pad] with zero padding.
+dfa_status launch_bwd_prep(dfa_dtype dt, int B, int H, int S, int S_pad, int D, const void* O,
+                           const void* dO, const float* lse, float* lse2, float* delta, cudaStream_t s);
 // out[x] = scale * acc[x] cast to dt, n elements.
 dfa_status launch_convert(dfa_dtype dt, int64_t n, float scale, const float* acc, void* out,
                           cudaStream_t s);
@@ -55,8 +59,10 @@ struct WorkList {
 };
 dfa_status tc_fwd(const AttnProblem& p, const void* q, const void* k, const void* v, void* O,
                   bool O_is_f32, float* lse, const WorkList* wl, cudaStream_t s);
+// lse2 = lse * log2(e) and delta are [B, H, S_pad] (S_pad = S rounded up to 128,
+// zero in the padding); dq_acc is fp32 [B, S, H, D] and must be zero.
 dfa_status tc_bwd(const AttnProblem& p, const void* q, const void* k, const void* v,
-                  const void* dO, const float* lse, const float* delta, float* dq_acc,
+                  const void* dO, const float* lse2, const float* delta, int S_pad, float* dq_acc,
                   void* dK, void* dV, const WorkList* wl, cudaStream_t s);
 
 int num_sms();

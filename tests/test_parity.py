@@ -168,6 +168,17 @@ def test_whole_sequence_matches_oracle(case):
     check_grads(grads, ref, dt, str(case))
 
 
+@pytest.mark.parametrize("k_scale", [2.0, 4.0])
+def test_sharp_softmax_exercises_the_lazy_rescale(k_scale):
+    """Large score ranges make the running max jump late in a row, so some rows
+    of a warp rescale their output accumulator while others do not."""
+    q, k, v, do = make(1, 4, 1, 2048, 128, torch.bfloat16, seed=23, device=DEV, k_scale=k_scale)
+    O, lse, grads = run_fwd_bwd(q, k, v, do, n_chunks=4)
+    Or, lr = oracle.attn_fwd(np64(q), np64(k), np64(v))
+    check_fwd(O, lse, Or, lr, torch.bfloat16, f"k x{k_scale}")
+    check_grads(grads, oracle.attn_bwd(np64(q), np64(k), np64(v), np64(do)), torch.bfloat16, f"k x{k_scale}")
+
+
 def test_non_causal_whole_sequence():
     q, k, v, do = make(1, 2, 1, 384, 128, torch.bfloat16, seed=9, device=DEV)
     O, lse, grads = run_fwd_bwd(q, k, v, do, causal=False)
