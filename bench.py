@@ -38,6 +38,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["dfa", "reference"], default="dfa")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--shape", default=None,
+                    help="B,H,H_kv,S,D: a custom bf16 shape instead of a named workload (profiling cases)")
     ap.add_argument("--sched", choices=["balanced", "unbalanced"], default="balanced")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -199,8 +201,13 @@ def run_reference(args, w):
 # ---------------------------------------------------------------- GPU arm
 def main():
     args = parse()
-    from long_context_causal_gb300.inputs import WORKLOADS
-    w = WORKLOADS[args.workload]
+    from long_context_causal_gb300.inputs import WORKLOADS, Workload
+    if args.shape:
+        import torch
+        B, H, Hkv, S, D = (int(x) for x in args.shape.split(","))
+        w = Workload(f"custom_B{B}_H{H}_Hkv{Hkv}_S{S}_D{D}", B, H, Hkv, S, D, 1, torch.bfloat16)
+    else:
+        w = WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)
         return

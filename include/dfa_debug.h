@@ -26,6 +26,18 @@ extern "C" {
  * Returns DFA_ERR_INVALID_ARG for an unknown form or bad pointers. */
 dfa_status dfa_debug_mma(int form, const void* A, const void* B, float* C, void* stream);
 
+/* Per-CTA timeline of the persistent attention kernels.  When `buf` is a
+ * device buffer of `capacity` records of 8 uint64, every later launch of the
+ * forward or backward kernel writes, for each CTA b < capacity,
+ *   buf[8b + 0] = SM id, [8b + 1] = start time (ns, %globaltimer),
+ *   [8b + 2] = end time (ns), [8b + 3] = work items in its list,
+ *   [8b + 4] = tiles its MMA thread processed, [8b + 5] = tiles its first
+ *   softmax/compute thread processed, [8b + 6] = tiles its producer loaded,
+ *   [8b + 7] = 0.
+ * Pass NULL to stop tracing.  The setting is process-wide; the caller owns
+ * the buffer and must keep it alive while tracing is on. */
+dfa_status dfa_debug_cta_trace(uint64_t* buf, int capacity);
+
 #ifdef __cplusplus
 }
 #endif

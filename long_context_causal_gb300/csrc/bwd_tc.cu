@@ -73,6 +73,8 @@ struct BwdArgs {
     const int32_t* wl_items;
     int n_units;                  // key tiles per (batch, kv head)
     int* err;
+    uint64_t* trace;              // optional per-CTA timeline (nullptr: off)
+    int trace_cap;
 };
 
 struct BItem {
@@ -162,6 +164,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    const uint64_t t_start = globaltimer();
     constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384;
 
     if (warp == 0) {
@@ -173,7 +176,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             return ok;
         };
         for (int it = it_begin; it < it_end && ok; ++it) {
-            const BItem x = bdecode(a, it);
+            const BItem x = bdecode(a, a.wl_items[it]);
             if (!wait(kv_empty, (kvi & 1) ^ 1)) break;
             ++kv_issued;
             if (lane == 0) {
@@ -221,6 +224,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             for (uint32_t m = (do_issued >= 2 ? do_issued - 2 : 0); m < do_issued; ++m)
                 mbar_wait(&do_full[m & 1], (m >> 1) & 1, &dummy, nullptr);
         }
+        if (lane == 0) trace_count(a.trace, a.trace_cap, 6, n);
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         const uint32_t idS = idesc_bf16_f32(BT, BT, false, false);     // S^T, dP^T
@@ -240,7 +244,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             __syncwarp();
         };
         for (int it = it_begin; it < it_end && ok; ++it) {
-            const BItem x = bdecode(a, it);
+            const BItem x = bdecode(a, a.wl_items[it]);
             if (!wait(kv_full, kvi & 1)) break;
             for (int k = 0; k < x.ntiles; ++k, ++n) {
                 const uint32_t s = n & 1, ph = (n >> 1) & 1;
@@ -300,6 +304,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         commit(done);
         int dummy = 0;
         mbar_wait(done, 0, &dummy, a.err);
+        if (lane == 0) trace_count(a.trace, a.trace_cap, 4, n);
     } else if (warp >= 4 && warp < 8) {
         // ------------------------------------------------------------ P^T / dS^T warpgroup
         const int r = (warp % 4) * 32 + lane;              // key row in the tile == TMEM lane
@@ -313,7 +318,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             return ok;
         };
         for (int it = it_begin; it < it_end && ok; ++it) {
-            const BItem x = bdecode(a, it);
+            const BItem x = bdecode(a, a.wl_items[it]);
             const int kvg = x.t * BT + r;                   // global key index of this thread's row
             const bool row_ok = kvg < a.S;
             for (int k = 0; k < x.ntiles; ++k, ++n) {
@@ -389,6 +394,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             mbar_arrive(kd_empty);
             ++kvi;
         }
+        if (threadIdx.x == 128) trace_count(a.trace, a.trace_cap, 5, n);
     } else if (warp >= 8) {
         // ------------------------------------------------------------ dQ drain warpgroup
         const int r = (warp % 4) * 32 + lane;              // query row in the tile == TMEM lane
@@ -396,7 +402,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         uint32_t n = 0;
         bool ok = true;
         for (int it = it_begin; it < it_end && ok; ++it) {
-            const BItem x = bdecode(a, it);
+            const BItem x = bdecode(a, a.wl_items[it]);
             for (int k = 0; k < x.ntiles; ++k, ++n) {
                 const int hh = k / (x.n_q - x.i0), i = x.i0 + k % (x.n_q - x.i0);
                 const int h = x.g * G + hh;
@@ -428,6 +434,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     __syncthreads();
     tc_fence_after();
     if (warp == 2) tmem_dealloc(tmem, 512);
+    if (threadIdx.x == 0) trace_cta(a.trace, a.trace_cap, t_start, it_end - it_begin);
 }
 
 template <int D>
@@ -448,6 +455,7 @@ dfa_status launch(const AttnProblem& p, const void* q, const void* k, const void
     a.dV = static_cast<__nv_bfloat16*>(dV);
     a.wl_offsets = wl->offsets; a.wl_items = wl->items; a.n_units = wl->n_units;
     a.err = device_error_flag();
+    a.trace = cta_trace(&a.trace_cap);
     auto kern = bwd_tc_kernel<D>;
     const int smem = BCfg<D>::kSmem;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)

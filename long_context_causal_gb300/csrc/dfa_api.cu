@@ -135,6 +135,16 @@ dfa_status fail(dfa_status st, const char* fmt, ...) {
 
 void count_launch(dfa_kernel_kind kind, int n) { g_launches[kind].fetch_add(n); }
 
+namespace {
+std::atomic<uint64_t*> g_trace{nullptr};
+std::atomic<int> g_trace_cap{0};
+}  // namespace
+
+uint64_t* cta_trace(int* capacity) {
+    *capacity = g_trace_cap.load();
+    return g_trace.load();
+}
+
 int* device_error_flag() {
     const int d = current_device();
     if (d < 0) return nullptr;
@@ -164,6 +174,14 @@ using namespace dfa;
 
 
 extern "C" const char* dfa_last_error(void) { return g_msg; }
+
+extern "C" dfa_status dfa_debug_cta_trace(uint64_t* buf, int capacity) {
+    if (buf && (capacity <= 0 || (reinterpret_cast<uintptr_t>(buf) & 7u)))
+        return fail(DFA_ERR_INVALID_ARG, "trace buffer needs capacity > 0 and 8-byte alignment");
+    g_trace_cap.store(buf ? capacity : 0);
+    g_trace.store(buf);
+    return DFA_OK;
+}
 
 extern "C" int64_t dfa_launch_count(dfa_kernel_kind kind) {
     if (kind < 0 || kind >= DFA_KERNEL_KINDS) return -1;

@@ -67,6 +67,8 @@ struct FwdArgs {
     const int32_t* wl_items;
     int n_units;
     int* err;
+    uint64_t* trace;              // optional per-CTA timeline (nullptr: off)
+    int trace_cap;
 };
 
 struct Item {
@@ -150,13 +152,14 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    const uint64_t t_start = globaltimer();
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         uint32_t ld = 0, qi = 0, qi_issued = 0;
         bool ok = true;
         for (int it = it_begin; it < it_end && ok; ++it) {
-            const Item x = decode(a, it);
+            const Item x = decode(a, a.wl_items ? a.wl_items[it] : it);
             if (x.n_kv == 0) continue;
             ok = __all_sync(0xffffffffu, mbar_wait(q_empty, (qi & 1) ^ 1, abort_flag, a.err));
             if (!ok) break;
@@ -196,6 +199,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             }
             if (qi_issued > 0) mbar_wait(q_full, (qi_issued - 1) & 1, &dummy, nullptr);
         }
+        if (lane == 0) trace_count(a.trace, a.trace_cap, 6, ld / 2);
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         const uint32_t idS = idesc_bf16_f32(BM, BN, false, false);
@@ -233,7 +237,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             __syncwarp();
         };
         for (int it = it_begin; it < it_end && ok; ++it) {
-            const Item x = decode(a, it);
+            const Item x = decode(a, a.wl_items ? a.wl_items[it] : it);
             if (x.n_kv == 0) continue;
             if (!wait(q_full, qi & 1)) break;
             uint32_t slotK = cons % C::kSlots;
@@ -276,6 +280,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         commit(done);
         int dummy = 0;
         mbar_wait(done, 0, &dummy, a.err);
+        if (lane == 0) trace_count(a.trace, a.trace_cap, 4, t);
     } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax warpgroups
         const int w = (warp - 4) / 4;                 // which query tile
@@ -287,7 +292,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         uint32_t t = 0, qi = 0;
         bool ok = true;
         for (int it = it_begin; it < it_end && ok; ++it) {
-            const Item x = decode(a, it);
+            const Item x = decode(a, a.wl_items ? a.wl_items[it] : it);
             const int row = x.q0 + w * BM + r;                 // row within the query chunk
             const int64_t qpos = a.q_offset + row;
             float m_run = -INFINITY, l = 0.f;
@@ -411,11 +416,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             if (valid_row)
                 a.lse[((int64_t)x.b * a.H + x.h) * a.Lq + row] = l > 0.f ? (m_run + __log2f(l)) * kLn2 : -INFINITY;
         }
+        if (threadIdx.x == 128) trace_count(a.trace, a.trace_cap, 5, t);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == 2) tmem_dealloc(tmem, 512);
+    if (threadIdx.x == 0) trace_cta(a.trace, a.trace_cap, t_start, it_end - it_begin);
 }
 
 // ---------------------------------------------------------------- host side
@@ -474,6 +481,7 @@ static dfa_status launch(const AttnProblem& p, const void* q, const void* k, con
     a.O = O; a.lse = lse;
     a.n_units = (p.Lq + kBlockRows - 1) / kBlockRows;
     a.err = device_error_flag();
+    a.trace = cta_trace(&a.trace_cap);
     int grid;
     if (wl) {
         a.wl_offsets = wl->offsets;

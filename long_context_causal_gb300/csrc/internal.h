@@ -73,6 +73,9 @@ int num_sms();
 bool make_tmap_bshd(void* map, const void* base, int B, int L, int heads, int D, int64_t sb,
                     int64_t ss, int64_t sh);
 
+// Per-CTA trace buffer set by dfa_debug_cta_trace (nullptr when off).
+uint64_t* cta_trace(int* capacity);
+
 // Host-side launch counters behind dfa_launch_count().
 void count_launch(dfa_kernel_kind kind, int n = 1);
 

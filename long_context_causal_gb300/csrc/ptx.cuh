@@ -27,6 +27,26 @@ __device__ __forceinline__ uint64_t globaltimer() {
     return t;
 }
 
+__device__ __forceinline__ uint32_t smid() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+    return r;
+}
+
+// Per-CTA trace record: SM, start, end, items, then three role counters.
+__device__ __forceinline__ void trace_cta(uint64_t* trace, int cap, uint64_t t_start, int items) {
+    if (trace && (int)blockIdx.x < cap) {
+        uint64_t* r = trace + 8 * blockIdx.x;
+        r[0] = smid();
+        r[1] = t_start;
+        r[2] = globaltimer();
+        r[3] = (uint64_t)items;
+    }
+}
+__device__ __forceinline__ void trace_count(uint64_t* trace, int cap, int slot, uint64_t v) {
+    if (trace && (int)blockIdx.x < cap) trace[8 * blockIdx.x + slot] = v;
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

@@ -54,6 +54,7 @@ def _load() -> ctypes.CDLL:
         "dfa_build_worklist": (i64, [i32, i32, i32, i32, p32, p32]),
         "dfa_chunk_schedule": (i32, [i32, i32, i32, p32]),
         "dfa_debug_mma": (i32, [i32, vp, vp, vp, vp]),
+        "dfa_debug_cta_trace": (i32, [vp, i32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -194,6 +195,15 @@ def dfa_debug_mma(form: int, A, B, C=None, stream=None):
     C = torch.empty((128, 128), dtype=torch.float32, device=A.device) if C is None else C
     _check(_lib.dfa_debug_mma(int(form), _ptr(A), _ptr(B), _ptr(C), _stream(stream)))
     return C
+
+
+def dfa_debug_cta_trace(buf=None):
+    """Turns the per-CTA timeline on (buf: int64 CUDA tensor of 8*n records) or off (None)."""
+    if buf is None:
+        _check(_lib.dfa_debug_cta_trace(None, 0))
+    else:
+        _check(_lib.dfa_debug_cta_trace(_ptr(buf), buf.numel() // 8))
+    return buf
 
 
 def dfa_check_errors(stream=None):
