@@ -118,6 +118,28 @@ dfa_status dfa_attn_bwd(const void* q, const void* k, const void* v, const void*
                         float scale, dfa_sched sched, void* dQ, void* dK, void* dV,
                         void* workspace, size_t ws_bytes, void* stream);
 
+/* dfa_attn_fwd for callers that cannot allocate device memory.  The paper
+ * has no counterpart to this entry point.  Some callers cannot call
+ * cudaMalloc where they run attention: a plugin whose host framework owns
+ * every byte of device memory, a service that forbids allocation once it is
+ * serving, code running while a stream is captured.  This variant takes no
+ * workspace: the per-CTA work list lives in a static device array of the
+ * library, 2^20 int32 entries (4 MiB) that every GPU which loads the library
+ * holds until the process exits.  Same arguments, layouts and results as
+ * dfa_attn_fwd without `workspace`/`ws_bytes`.
+ *  - Limit: B*H*ceil(S/256) must not exceed 2^20 - 1025 work items; larger
+ *    problems return DFA_ERR_INVALID_ARG without launching anything.
+ *  - Set-up: the first bf16 call on a device looks up the array's device
+ *    address (with that device current); make that first call before any
+ *    stream capture.
+ *  - The array is shared by all calls and keeps the last call's contents;
+ *    each call rewrites what it uses.  Calls that overlap on the GPU (other
+ *    streams or host threads) race on it: serialise them.
+ *  - It allocates nothing: no cudaMalloc, cudaFree or other allocating call. */
+dfa_status dfa_attn_fwd_noalloc(const void* q, const void* k, const void* v, dfa_dtype dt,
+                                int B, int H, int H_kv, int S, int D, int n_chunks, int causal,
+                                float scale, dfa_sched sched, void* O, float* lse, void* stream);
+
 /* Synchronises `stream`, then reports and clears the device error flag:
  * DFA_ERR_TIMEOUT if a kernel gave up on a bounded wait, DFA_ERR_CUDA if the
  * stream holds a CUDA error, DFA_OK otherwise. */

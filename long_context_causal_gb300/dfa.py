@@ -48,6 +48,7 @@ def _load() -> ctypes.CDLL:
         "dfa_attn_fwd": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, f32, i32, vp, vp, vp, sz, vp]),
         "dfa_attn_bwd": (i32, [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, f32, i32,
                                vp, vp, vp, vp, sz, vp]),
+        "dfa_attn_fwd_noalloc": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, f32, i32, vp, vp, vp]),
         "dfa_check_errors": (i32, [vp]),
         "dfa_last_error": (ctypes.c_char_p, []),
         "dfa_launch_count": (i64, [i32]),
@@ -168,6 +169,20 @@ def dfa_attn_fwd(q, k, v, n_chunks: int = 1, causal: bool = True, scale: float |
     _check(_lib.dfa_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _dtype(q), B, H, Hkv, S, D, int(n_chunks),
                              int(bool(causal)), scale, _SCHED[sched], _ptr(O), _ptr(lse), _ptr(ws),
                              ws.numel(), _stream(stream)))
+    return O, lse
+
+
+def dfa_attn_fwd_noalloc(q, k, v, O, lse, n_chunks: int = 1, causal: bool = True,
+                         scale: float | None = None, sched="balanced", stream=None):
+    """dfa_attn_fwd without a workspace: writes the caller's O and lse, allocates nothing."""
+    B, S, H, D = q.shape
+    Hkv = k.shape[2]
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (O, "O"), (lse, "lse")):
+        _dense(t, n)
+    scale = D ** -0.5 if scale is None else float(scale)
+    _check(_lib.dfa_attn_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _dtype(q), B, H, Hkv, S, D, int(n_chunks),
+                                     int(bool(causal)), scale, _SCHED[sched], _ptr(O), _ptr(lse),
+                                     _stream(stream)))
     return O, lse
 
 
