@@ -33,7 +33,7 @@ dfa_status dfa_debug_mma(int form, const void* A, const void* B, float* C, void*
  *   [8b + 2] = end time (ns), [8b + 3] = work items in its list,
  *   [8b + 4] = tiles its MMA thread processed, [8b + 5] = tiles its first
  *   softmax/compute thread processed, [8b + 6] = tiles its producer loaded,
- *   [8b + 7] = 0.
+ *   [8b + 7] = tiles its dQ drain warpgroup processed (backward; 0 forward).
  * Pass NULL to stop tracing.  The setting is process-wide; the caller owns
  * the buffer and must keep it alive while tracing is on. */
 dfa_status dfa_debug_cta_trace(uint64_t* buf, int capacity);

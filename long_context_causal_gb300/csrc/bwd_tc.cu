@@ -18,15 +18,16 @@
 //               plus the query tile's lse and Delta (bulk copies).
 //   warp 1      MMA issuer (one thread), per query tile:
 //                 S^T = K Q^T, dP^T = V dO^T, dV += P^T dO, dK += dS^T Q,
-//                 dQ = dS K.
+//                 dQ = dS K (stored transposed, dQ^T = K^T dS^T, for D = 128).
 //   warp 2      TMEM allocation.
 //   warps 4-7   one key row per thread: P^T = exp2(S^T c - lse2),
 //               dS^T = P^T (dP^T - Delta); P^T (bf16) back into TMEM over S^T,
 //               dS^T (bf16) into swizzled shared memory where it serves as the
 //               K-major A operand of dK and the M-major A operand of dQ; at the
 //               end of an item the dK/dV epilogue.
-//   warps 8-11  one query row per thread: dQ partial out of TMEM, then
-//               vectorised fp32 atomic adds into the accumulator.
+//   warps 8-11  dQ partial out of TMEM, then fp32 atomic adds into the
+//               accumulator (D = 128: one head-dim element per thread, so a
+//               warp's adds cover 128 contiguous bytes of one dQ row).
 //
 // TMEM columns: dV [0,128) dK [128,256) S^T/P^T [256,384) dP^T/dQ [384,512).
 #include <cuda.h>
@@ -229,7 +230,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         // ------------------------------------------------------------ MMA issuer
         const uint32_t idS = idesc_bf16_f32(BT, BT, false, false);     // S^T, dP^T
         const uint32_t idKM = idesc_bf16_f32(BT, D, false, true);      // dV, dK: A K-major, B N-major
-        const uint32_t idQ = idesc_bf16_f32(BT, D, true, true);        // dQ: A M-major, B N-major
+        // dQ (D = 64): M = query rows; dQ^T (D = 128): M = head dim.  A, B both MN-major.
+        const uint32_t idQ = D == 128 ? idesc_bf16_f32(D, BT, true, true) : idesc_bf16_f32(BT, D, true, true);
         const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), adO = smem_u32(sdO),
                        adS = smem_u32(sdS);
         uint32_t n = 0, kvi = 0;
@@ -287,10 +289,20 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 }
                 commit(&q_empty[s]);
                 if (lane == 0) {
+                    if constexpr (D == 128) {
+                        // dQ^T = K^T dS^T (M = head dim, N = query rows): the head
+                        // dimension lands on TMEM lanes, so each warp of the drain
+                        // warpgroup adds one contiguous 128-byte piece of a dQ row.
 #pragma unroll
-                    for (int kk = 0; kk < BT / 16; ++kk)   // dQ = dS K
-                        mma_ss(tmem + kColDP, sdesc_sw128(adS + kk * 2048, 16384, 1024),
-                               sdesc_sw128(aK + kk * 2048, 16384, 1024), idQ, kk > 0);
+                        for (int kk = 0; kk < BT / 16; ++kk)
+                            mma_ss(tmem + kColDP, sdesc_sw128(aK + kk * 2048, 16384, 1024),
+                                   sdesc_sw128(adS + kk * 2048, 16384, 1024), idQ, kk > 0);
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < BT / 16; ++kk)   // dQ = dS K
+                            mma_ss(tmem + kColDP, sdesc_sw128(adS + kk * 2048, 16384, 1024),
+                                   sdesc_sw128(aK + kk * 2048, 16384, 1024), idQ, kk > 0);
+                    }
                 }
                 commit(dq_full);
                 if (k == x.ntiles - 1) {
@@ -397,8 +409,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         if (threadIdx.x == 128) trace_count(a.trace, a.trace_cap, 5, n);
     } else if (warp >= 8) {
         // ------------------------------------------------------------ dQ drain warpgroup
-        const int r = (warp % 4) * 32 + lane;              // query row in the tile == TMEM lane
+        // TMEM lane r = head-dim element r of dQ^T (D = 128) or query row r of dQ (D = 64).
+        const int r = (warp % 4) * 32 + lane;
         const uint32_t tdQ = tmem + ((uint32_t)((warp % 4) * 32) << 16) + kColDP;
+        constexpr int kCols = D == 128 ? BT : D;
         uint32_t n = 0;
         bool ok = true;
         for (int it = it_begin; it < it_end && ok; ++it) {
@@ -409,9 +423,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 ok = __all_sync(0xffffffffu, mbar_wait(dq_full, n & 1, abort_flag, a.err));
                 if (!ok) break;
                 tc_fence_after();
-                uint32_t u[D];
+                uint32_t u[kCols];
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < kCols / 32; ++c) {
                     uint32_t t32[32];
                     tmem_ld32(tdQ + c * 32, t32);
 #pragma unroll
@@ -419,16 +433,26 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 }
                 tc_fence_before();
                 mbar_arrive(dq_free);
-                const int qg = i * BT + r;
-                if (qg < a.S) {
-                    float4* dst = reinterpret_cast<float4*>(a.dq_acc + (((int64_t)x.b * a.S + qg) * a.H + h) * D);
+                if constexpr (D == 128) {
+                    // Column c is query row i*128 + c: the warp adds 32 consecutive floats of it.
+                    float* base = a.dq_acc + ((int64_t)x.b * a.S + (int64_t)i * BT) * a.H * D + (int64_t)h * D + r;
+                    const int nq = min(BT, a.S - i * BT);
 #pragma unroll
-                    for (int e = 0; e < D / 4; ++e)
-                        atomicAdd(dst + e, make_float4(__uint_as_float(u[4 * e]), __uint_as_float(u[4 * e + 1]),
-                                                       __uint_as_float(u[4 * e + 2]), __uint_as_float(u[4 * e + 3])));
+                    for (int c = 0; c < BT; ++c)
+                        if (c < nq) atomicAdd(base + (int64_t)c * a.H * D, __uint_as_float(u[c]));
+                } else {
+                    const int qg = i * BT + r;
+                    if (qg < a.S) {
+                        float4* dst = reinterpret_cast<float4*>(a.dq_acc + (((int64_t)x.b * a.S + qg) * a.H + h) * D);
+#pragma unroll
+                        for (int e = 0; e < D / 4; ++e)
+                            atomicAdd(dst + e, make_float4(__uint_as_float(u[4 * e]), __uint_as_float(u[4 * e + 1]),
+                                                           __uint_as_float(u[4 * e + 2]), __uint_as_float(u[4 * e + 3])));
+                    }
                 }
             }
         }
+        if (threadIdx.x == 256) trace_count(a.trace, a.trace_cap, 7, n);
     }
     tc_fence_before();
     __syncthreads();

@@ -94,6 +94,52 @@ __device__ __forceinline__ Item decode(const FwdArgs& a, int it) {
     return x;
 }
 
+// Row max of this thread's 128 scores in TMEM (columns >= lim masked when MASK).
+// Four independent accumulators keep the dependent chain short.
+template <bool MASK>
+__device__ __forceinline__ float row_max(uint32_t tS, int lim) {
+    float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+        uint32_t u[32];
+        tmem_ld32(tS + c * 32, u);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            const float x = __uint_as_float(u[e]);
+            m[e & 3] = fmaxf(m[e & 3], (!MASK || c * 32 + e < lim) ? x : -INFINITY);
+        }
+    }
+    return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+}
+
+// P = exp2(s * c2 - m) for this thread's row, written as bf16 pairs over the
+// first 64 TMEM columns of S (behind the columns still to be read).  Returns
+// the row sum of the fp32 P values.
+template <bool MASK>
+__device__ __forceinline__ float row_exp(uint32_t tS, int lim, float c2, float m) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+        uint32_t u[32];
+        tmem_ld32(tS + c * 32, u);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int c0 = c * 32 + 2 * e;
+            float p0 = ex2(fmaf(__uint_as_float(u[2 * e]), c2, -m));
+            float p1 = ex2(fmaf(__uint_as_float(u[2 * e + 1]), c2, -m));
+            if (MASK) {
+                p0 = c0 < lim ? p0 : 0.f;
+                p1 = c0 + 1 < lim ? p1 : 0.f;
+            }
+            acc[e & 3] += p0 + p1;
+            pk[e] = pack_bf16(p0, p1);
+        }
+        tmem_st16(tS + c * 16, pk);
+    }
+    return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+}
+
 template <int D, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -315,15 +361,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     }
                     lim = v < 0 ? 0 : (v > BN ? BN : (int)v);
                 }
-                float mx = -INFINITY;
-#pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t u[32];
-                    tmem_ld32(tS + c * 32, u);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        mx = fmaxf(mx, (c * 32 + e < lim) ? __uint_as_float(u[e]) : -INFINITY);
-                }
+                const float mx = masked ? row_max<true>(tS, lim) : row_max<false>(tS, lim);
                 const float mx2 = mx * c2;
                 // Lazy rescale: move this row's reference max only when the tile
                 // max exceeds it by more than 2^8.  The decision is per row, but
@@ -351,21 +389,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 }
                 const float m_use = m_run == -INFINITY ? 0.f : m_run;
                 // Pass 2: P = exp2(s * c2 - m), row sum, bf16 P written over S.
-#pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t u[32];
-                    tmem_ld32(tS + c * 32, u);
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int c0 = c * 32 + 2 * e;
-                        const float p0 = c0 < lim ? ex2(fmaf(__uint_as_float(u[2 * e]), c2, -m_use)) : 0.f;
-                        const float p1 = c0 + 1 < lim ? ex2(fmaf(__uint_as_float(u[2 * e + 1]), c2, -m_use)) : 0.f;
-                        l += p0 + p1;
-                        pk[e] = pack_bf16(p0, p1);
-                    }
-                    tmem_st16(tS + c * 16, pk);
-                }
+                l += masked ? row_exp<true>(tS, lim, c2, m_use) : row_exp<false>(tS, lim, c2, m_use);
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(&p_full[w]);

@@ -16,7 +16,8 @@ import re
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libdfa.so")
+# DFA_LIB_PATH selects another build of the same library (e.g. a profiling build).
+LIB_PATH = os.environ.get("DFA_LIB_PATH") or os.path.join(_PKG, "libdfa.so")
 INCLUDE = os.path.join(os.path.dirname(_PKG), "include")
 HEADER = os.path.join(INCLUDE, "dfa.h")
 
