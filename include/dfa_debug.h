@@ -27,13 +27,18 @@ extern "C" {
 dfa_status dfa_debug_mma(int form, const void* A, const void* B, float* C, void* stream);
 
 /* Per-CTA timeline of the persistent attention kernels.  When `buf` is a
- * device buffer of `capacity` records of 8 uint64, every later launch of the
- * forward or backward kernel writes, for each CTA b < capacity,
+ * device buffer of 16 x `capacity` uint64, every later launch of the
+ * forward or backward kernel writes, for each CTA b < capacity, a record
  *   buf[8b + 0] = SM id, [8b + 1] = start time (ns, %globaltimer),
  *   [8b + 2] = end time (ns), [8b + 3] = work items in its list,
  *   [8b + 4] = tiles its MMA thread processed, [8b + 5] = tiles its first
  *   softmax/compute thread processed, [8b + 6] = tiles its producer loaded,
- *   [8b + 7] = tiles its dQ drain warpgroup processed (backward; 0 forward).
+ *   [8b + 7] = tiles its dQ drain warpgroup processed (backward; 0 forward),
+ * and a wait profile at buf[8 capacity + 8b + slot]: SM clock cycles each
+ * role spent blocked on barriers.  Backward slots: 0 producer (free slots), 1 MMA
+ * on tile loads, 2 MMA on the dQ drain, 3 MMA on P/dS, 4 MMA on K/V and the
+ * dK/dV epilogue, 5 P/dS warpgroup on its tile inputs, 6 P/dS warpgroup on
+ * the dK/dV accumulators, 7 dQ drain on the dQ MMA.  Forward: 0.
  * Pass NULL to stop tracing.  The setting is process-wide; the caller owns
  * the buffer and must keep it alive while tracing is on. */
 dfa_status dfa_debug_cta_trace(uint64_t* buf, int capacity);

@@ -172,8 +172,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         // ------------------------------------------------------------ TMA producer
         uint32_t n = 0, kvi = 0, kv_issued = 0, q_issued = 0, do_issued = 0;
         bool ok = true;
+        uint64_t wt = 0;
         auto wait = [&](uint64_t* bar, uint32_t parity) {
-            ok = ok && __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, a.err));
+            ok = ok && __all_sync(0xffffffffu, mbar_wait_acc(bar, parity, abort_flag, a.err, a.trace ? &wt : nullptr));
             return ok;
         };
         for (int it = it_begin; it < it_end && ok; ++it) {
@@ -225,19 +226,32 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             for (uint32_t m = (do_issued >= 2 ? do_issued - 2 : 0); m < do_issued; ++m)
                 mbar_wait(&do_full[m & 1], (m >> 1) & 1, &dummy, nullptr);
         }
-        if (lane == 0) trace_count(a.trace, a.trace_cap, 6, n);
+        if (lane == 0) {
+            trace_count(a.trace, a.trace_cap, 6, n);
+            trace_wait(a.trace, a.trace_cap, 0, wt);
+        }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         const uint32_t idS = idesc_bf16_f32(BT, BT, false, false);     // S^T, dP^T
         const uint32_t idKM = idesc_bf16_f32(BT, D, false, true);      // dV, dK: A K-major, B N-major
         // dQ (D = 64): M = query rows; dQ^T (D = 128): M = head dim.  A, B both MN-major.
         const uint32_t idQ = D == 128 ? idesc_bf16_f32(D, BT, true, true) : idesc_bf16_f32(BT, D, true, true);
-        const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), adO = smem_u32(sdO),
-                       adS = smem_u32(sdS);
+        // Descriptors are built once and advanced by adding (byte offset / 16)
+        // (start-address field = addr >> 4, shared addresses < 256 KB): a short
+        // issue loop is what lets one thread keep the tensor core busy.
+        const uint64_t dKk = sdesc_sw128(smem_u32(sK), 16, 1024), dKn = sdesc_sw128(smem_u32(sK), 16384, 1024);
+        const uint64_t dVk = sdesc_sw128(smem_u32(sV), 16, 1024);
+        const uint64_t dQk = sdesc_sw128(smem_u32(sQ), 16, 1024), dQn = sdesc_sw128(smem_u32(sQ), 16384, 1024);
+        const uint64_t dOk = sdesc_sw128(smem_u32(sdO), 16, 1024), dOn = sdesc_sw128(smem_u32(sdO), 16384, 1024);
+        const uint64_t dSk = sdesc_sw128(smem_u32(sdS), 16, 1024), dSn = sdesc_sw128(smem_u32(sdS), 16384, 1024);
+        constexpr uint64_t kSlot = C::kTile >> 4, kRows16 = 2048 >> 4;
+        auto kmaj = [](int kk) -> uint64_t { return (uint64_t)(((kk / 4) * 16384 + (kk % 4) * 32) >> 4); };
         uint32_t n = 0, kvi = 0;
         bool ok = true;
-        auto wait = [&](uint64_t* bar, uint32_t parity) {
-            ok = ok && __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, a.err));
+        uint64_t wt[4] = {0, 0, 0, 0};   // loads, dq_free, pds_full, kv_full + kd_empty
+        auto wait = [&](uint64_t* bar, uint32_t parity, int slot) {
+            ok = ok && __all_sync(0xffffffffu,
+                                  mbar_wait_acc(bar, parity, abort_flag, a.err, a.trace ? &wt[slot] : nullptr));
             if (ok) tc_fence_after();
             return ok;
         };
@@ -247,45 +261,39 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         };
         for (int it = it_begin; it < it_end && ok; ++it) {
             const BItem x = bdecode(a, a.wl_items[it]);
-            if (!wait(kv_full, kvi & 1)) break;
+            if (!wait(kv_full, kvi & 1, 3)) break;
             for (int k = 0; k < x.ntiles; ++k, ++n) {
                 const uint32_t s = n & 1, ph = (n >> 1) & 1;
-                const uint32_t q = aQ + s * C::kTile, dO = adO + s * C::kTile;
-                if (!wait(&q_full[s], ph)) break;
-                if (lane == 0) {
+                if (!wait(&q_full[s], ph, 0)) break;
+                if (lane == 0) {   // S^T = K Q^T
+                    const uint64_t b0 = dQk + s * kSlot;
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-                        mma_ss(tmem + kColS, sdesc_sw128(aK + off, 16, 1024), sdesc_sw128(q + off, 16, 1024), idS,
-                               kk > 0);
-                    }
+                    for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + kColS, dKk + kmaj(kk), b0 + kmaj(kk), idS, kk > 0);
                 }
                 commit(s_full);
-                if (!wait(&do_full[s], ph)) break;
-                if (n > 0 && !wait(dq_free, (n - 1) & 1)) break;
-                if (lane == 0) {
+                if (!wait(&do_full[s], ph, 0)) break;
+                if (n > 0 && !wait(dq_free, (n - 1) & 1, 1)) break;
+                if (lane == 0) {   // dP^T = V dO^T
+                    const uint64_t b0 = dOk + s * kSlot;
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-                        mma_ss(tmem + kColDP, sdesc_sw128(aV + off, 16, 1024), sdesc_sw128(dO + off, 16, 1024), idS,
-                               kk > 0);
-                    }
+                    for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + kColDP, dVk + kmaj(kk), b0 + kmaj(kk), idS, kk > 0);
                 }
                 commit(dp_full);
-                if (k == 0 && !wait(kd_empty, (kvi & 1) ^ 1)) break;
-                if (!wait(pds_full, n & 1)) break;
-                if (lane == 0) {
+                if (k == 0 && !wait(kd_empty, (kvi & 1) ^ 1, 3)) break;
+                if (!wait(pds_full, n & 1, 2)) break;
+                const uint32_t acc0 = k > 0 ? 1u : 0u;
+                if (lane == 0) {   // dV += P^T dO
+                    const uint64_t b0 = dOn + s * kSlot;
 #pragma unroll
-                    for (int kk = 0; kk < BT / 16; ++kk)   // dV += P^T dO
-                        mma_ts(tmem + kColDV, tmem + kColS + kk * 8, sdesc_sw128(dO + kk * 2048, 16384, 1024), idKM,
-                               (k > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < BT / 16; ++kk)
+                        mma_ts(tmem + kColDV, tmem + kColS + kk * 8, b0 + kk * kRows16, idKM, kk > 0 ? 1u : acc0);
                 }
                 commit(&do_empty[s]);
-                if (lane == 0) {
+                if (lane == 0) {   // dK += dS^T Q
+                    const uint64_t b0 = dQn + s * kSlot;
 #pragma unroll
-                    for (int kk = 0; kk < BT / 16; ++kk)   // dK += dS^T Q
-                        mma_ss(tmem + kColDK, sdesc_sw128(adS + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024),
-                               sdesc_sw128(q + kk * 2048, 16384, 1024), idKM, (k > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < BT / 16; ++kk)
+                        mma_ss(tmem + kColDK, dSk + kmaj(kk), b0 + kk * kRows16, idKM, kk > 0 ? 1u : acc0);
                 }
                 commit(&q_empty[s]);
                 if (lane == 0) {
@@ -295,13 +303,11 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                         // warpgroup adds one contiguous 128-byte piece of a dQ row.
 #pragma unroll
                         for (int kk = 0; kk < BT / 16; ++kk)
-                            mma_ss(tmem + kColDP, sdesc_sw128(aK + kk * 2048, 16384, 1024),
-                                   sdesc_sw128(adS + kk * 2048, 16384, 1024), idQ, kk > 0);
+                            mma_ss(tmem + kColDP, dKn + kk * kRows16, dSn + kk * kRows16, idQ, kk > 0);
                     } else {
 #pragma unroll
                         for (int kk = 0; kk < BT / 16; ++kk)   // dQ = dS K
-                            mma_ss(tmem + kColDP, sdesc_sw128(adS + kk * 2048, 16384, 1024),
-                                   sdesc_sw128(aK + kk * 2048, 16384, 1024), idQ, kk > 0);
+                            mma_ss(tmem + kColDP, dSn + kk * kRows16, dKn + kk * kRows16, idQ, kk > 0);
                     }
                 }
                 commit(dq_full);
@@ -316,7 +322,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         commit(done);
         int dummy = 0;
         mbar_wait(done, 0, &dummy, a.err);
-        if (lane == 0) trace_count(a.trace, a.trace_cap, 4, n);
+        if (lane == 0) {
+            trace_count(a.trace, a.trace_cap, 4, n);
+            for (int z = 0; z < 4; ++z) trace_wait(a.trace, a.trace_cap, 1 + z, wt[z]);
+        }
     } else if (warp >= 4 && warp < 8) {
         // ------------------------------------------------------------ P^T / dS^T warpgroup
         const int r = (warp % 4) * 32 + lane;              // key row in the tile == TMEM lane
@@ -325,8 +334,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const uint32_t tdP = tmem + lane_base + kColDP;
         uint32_t n = 0, kvi = 0;
         bool ok = true;
-        auto wait = [&](uint64_t* bar, uint32_t parity) {
-            ok = ok && __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, a.err));
+        uint64_t wt[2] = {0, 0};   // tile inputs (q_full, s_full, dp_full), kd_full
+        auto wait = [&](uint64_t* bar, uint32_t parity, int slot) {
+            ok = ok && __all_sync(0xffffffffu,
+                                  mbar_wait_acc(bar, parity, abort_flag, a.err, a.trace ? &wt[slot] : nullptr));
             return ok;
         };
         for (int it = it_begin; it < it_end && ok; ++it) {
@@ -336,7 +347,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             for (int k = 0; k < x.ntiles; ++k, ++n) {
                 const int i = x.i0 + k % (x.n_q - x.i0);
                 const uint32_t s = n & 1, ph = (n >> 1) & 1;
-                if (!wait(&q_full[s], ph) || !wait(s_full, n & 1) || !wait(dp_full, n & 1)) break;
+                if (!wait(&q_full[s], ph, 0) || !wait(s_full, n & 1, 0) || !wait(dp_full, n & 1, 0)) break;
                 tc_fence_after();
                 const float* lse2 = reinterpret_cast<const float*>(sSide + s * kSide);
                 const float* dl = lse2 + BT;
@@ -344,22 +355,26 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 #pragma unroll 1
                 for (int c = 0; c < BT / 32; ++c) {
                     uint32_t us[32], ud[32];
-                    tmem_ld32(tS + c * 32, us);
-                    tmem_ld32(tdP + c * 32, ud);
+                    tmem_ld32x2(tS + c * 32, tdP + c * 32, us, ud);   // one round trip for both
                     uint32_t pk[16], dk[16];
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        float pp[2], dd[2];
+                    for (int e = 0; e < 32; e += 4) {
+                        const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c * 32 + e);
+                        const float4 d4 = *reinterpret_cast<const float4*>(dl + c * 32 + e);
+                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+                        float pp[4], dd[4];
 #pragma unroll
-                        for (int z = 0; z < 2; ++z) {
-                            const int qc = c * 32 + e + z, qg = q0 + qc;
+                        for (int z = 0; z < 4; ++z) {
+                            const int qg = q0 + c * 32 + e + z;
                             const bool vis = row_ok && qg < a.S && !(a.causal && kvg > qg);
-                            const float p = vis ? ex2(fmaf(__uint_as_float(us[e + z]), a.c2, -lse2[qc])) : 0.f;
+                            const float p = vis ? ex2(fmaf(__uint_as_float(us[e + z]), a.c2, -lv[z])) : 0.f;
                             pp[z] = p;
-                            dd[z] = p * (__uint_as_float(ud[e + z]) - dl[qc]);
+                            dd[z] = p * (__uint_as_float(ud[e + z]) - dv[z]);
                         }
                         pk[e / 2] = pack_bf16(pp[0], pp[1]);
+                        pk[e / 2 + 1] = pack_bf16(pp[2], pp[3]);
                         dk[e / 2] = pack_bf16(dd[0], dd[1]);
+                        dk[e / 2 + 1] = pack_bf16(dd[2], dd[3]);
                     }
                     tmem_st16(tP + c * 16, pk);
                     uint8_t* blk = sdS + (c / 2) * 16384;
@@ -375,7 +390,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             }
             if (!ok) break;
             // ---- epilogue: dV = acc, dK = scale * acc, bf16, [B, S, Hkv, D]
-            if (!wait(kd_full, kvi & 1)) break;
+            if (!wait(kd_full, kvi & 1, 1)) break;
             tc_fence_after();
             const int64_t orow = (((int64_t)x.b * a.S + kvg) * a.Hkv + x.g) * D;
 #pragma unroll 1
@@ -406,7 +421,11 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             mbar_arrive(kd_empty);
             ++kvi;
         }
-        if (threadIdx.x == 128) trace_count(a.trace, a.trace_cap, 5, n);
+        if (threadIdx.x == 128) {
+            trace_count(a.trace, a.trace_cap, 5, n);
+            trace_wait(a.trace, a.trace_cap, 5, wt[0]);
+            trace_wait(a.trace, a.trace_cap, 6, wt[1]);
+        }
     } else if (warp >= 8) {
         // ------------------------------------------------------------ dQ drain warpgroup
         // TMEM lane r = head-dim element r of dQ^T (D = 128) or query row r of dQ (D = 64).
@@ -415,12 +434,13 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         constexpr int kCols = D == 128 ? BT : D;
         uint32_t n = 0;
         bool ok = true;
+        uint64_t wt = 0;
         for (int it = it_begin; it < it_end && ok; ++it) {
             const BItem x = bdecode(a, a.wl_items[it]);
             for (int k = 0; k < x.ntiles; ++k, ++n) {
                 const int hh = k / (x.n_q - x.i0), i = x.i0 + k % (x.n_q - x.i0);
                 const int h = x.g * G + hh;
-                ok = __all_sync(0xffffffffu, mbar_wait(dq_full, n & 1, abort_flag, a.err));
+                ok = __all_sync(0xffffffffu, mbar_wait_acc(dq_full, n & 1, abort_flag, a.err, a.trace ? &wt : nullptr));
                 if (!ok) break;
                 tc_fence_after();
                 uint32_t u[kCols];
@@ -452,7 +472,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 }
             }
         }
-        if (threadIdx.x == 256) trace_count(a.trace, a.trace_cap, 7, n);
+        if (threadIdx.x == 256) {
+            trace_count(a.trace, a.trace_cap, 7, n);
+            trace_wait(a.trace, a.trace_cap, 7, wt);
+        }
     }
     tc_fence_before();
     __syncthreads();

@@ -95,7 +95,9 @@ __device__ __forceinline__ Item decode(const FwdArgs& a, int it) {
 }
 
 // Row max of this thread's 128 scores in TMEM (columns >= lim masked when MASK).
-// Four independent accumulators keep the dependent chain short.
+// Four independent accumulators keep the dependent chain short; the chunk
+// loop stays rolled to keep the kernel's code small (several roles run
+// different code at once and share the instruction cache).
 template <bool MASK>
 __device__ __forceinline__ float row_max(uint32_t tS, int lim) {
     float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -207,7 +209,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         for (int it = it_begin; it < it_end && ok; ++it) {
             const Item x = decode(a, a.wl_items ? a.wl_items[it] : it);
             if (x.n_kv == 0) continue;
-            ok = __all_sync(0xffffffffu, mbar_wait(q_empty, (qi & 1) ^ 1, abort_flag, a.err));
+            ok = __all_sync(0xffffffffu, mbar_wait_acc(q_empty, (qi & 1) ^ 1, abort_flag, a.err, nullptr));
             if (!ok) break;
             ++qi_issued;
             if (lane == 0) {
@@ -221,8 +223,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             for (int j = 0; j < x.n_kv && ok; ++j) {
                 for (int which = 0; which < 2; ++which, ++ld) {
                     const int slot = ld % C::kSlots;
-                    ok = __all_sync(0xffffffffu, mbar_wait(&kv_empty[slot], ((ld / C::kSlots) & 1) ^ 1,
-                                                           abort_flag, a.err));
+                    ok = __all_sync(0xffffffffu, mbar_wait_acc(&kv_empty[slot], ((ld / C::kSlots) & 1) ^ 1,
+                                                               abort_flag, a.err, nullptr));
                     if (!ok) break;
                     if (lane == 0) {
                         mbar_arrive_expect_tx(&kv_full[slot], C::kTileBytes);
@@ -250,31 +252,38 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         // ------------------------------------------------------------ MMA issuer
         const uint32_t idS = idesc_bf16_f32(BM, BN, false, false);
         const uint32_t idO = idesc_bf16_f32(BM, D, false, true);
-        const uint32_t qaddr = smem_u32(sQ), kvaddr = smem_u32(sKV);
+        // Descriptors are built once and advanced by adding (byte offset / 16):
+        // the start-address field is addr >> 4 and shared addresses stay below
+        // 256 KB, so the addition never carries out of the field.  Keeping the
+        // issue loop this short is what lets one thread feed the tensor core.
+        const uint64_t dQk = sdesc_sw128(smem_u32(sQ), 16, 1024);          // Q, K-major
+        const uint64_t dKk = sdesc_sw128(smem_u32(sKV), 16, 1024);         // K slots, K-major
+        const uint64_t dVn = sdesc_sw128(smem_u32(sKV), 16384, 1024);      // V slots, N-major
+        constexpr uint64_t kSlotStep = C::kTileBytes >> 4;
         uint32_t cons = 0, t = 0, qi = 0;
         bool ok = true;
         auto issue_S = [&](int w, uint32_t slot) {
             if (lane == 0) {
+                const uint64_t a0 = dQk + w * kSlotStep, b0 = dKk + slot * kSlotStep;
+                const uint32_t d = tmem + w * 128;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-                    mma_ss(tmem + w * 128, sdesc_sw128(qaddr + w * C::kTileBytes + off, 16, 1024),
-                           sdesc_sw128(kvaddr + slot * C::kTileBytes + off, 16, 1024), idS, kk > 0);
+                    const uint64_t off = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
+                    mma_ss(d, a0 + off, b0 + off, idS, kk > 0);
                 }
             }
         };
         auto issue_PV = [&](int w, uint32_t slot, bool acc) {
             if (lane == 0) {
+                const uint64_t b0 = dVn + slot * kSlotStep;
+                const uint32_t d = tmem + 256 + w * 128, a = tmem + w * 128;
+                mma_ts(d, a, b0, idO, acc ? 1u : 0u);
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    mma_ts(tmem + 256 + w * 128, tmem + w * 128 + kk * 8,
-                           sdesc_sw128(kvaddr + slot * C::kTileBytes + kk * 2048, 16384, 1024), idO,
-                           (acc || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 1; kk < BN / 16; ++kk) mma_ts(d, a + kk * 8, b0 + kk * (2048 >> 4), idO, 1u);
             }
         };
         auto wait = [&](uint64_t* bar, uint32_t parity) {
-            ok = ok && __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, a.err));
+            ok = ok && __all_sync(0xffffffffu, mbar_wait_acc(bar, parity, abort_flag, a.err, nullptr));
             if (ok) tc_fence_after();
             return ok;
         };
@@ -343,7 +352,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             const int64_t qpos = a.q_offset + row;
             float m_run = -INFINITY, l = 0.f;
             for (int j = 0; j < x.n_kv; ++j, ++t) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&s_full[w], t & 1, abort_flag, a.err));
+                ok = __all_sync(0xffffffffu, mbar_wait_acc(&s_full[w], t & 1, abort_flag, a.err, nullptr));
                 if (!ok) break;
                 tc_fence_after();
                 // Pass 1: row max over the tile (S read from TMEM 32 columns at a time).
@@ -400,7 +409,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const int64_t orow = (((int64_t)x.b * a.Lq + row) * a.H + x.h) * D;
             if (x.n_kv > 0) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&o_full[w], qi & 1, abort_flag, a.err));
+                ok = __all_sync(0xffffffffu, mbar_wait_acc(&o_full[w], qi & 1, abort_flag, a.err, nullptr));
                 if (!ok) break;
                 tc_fence_after();
                 ++qi;

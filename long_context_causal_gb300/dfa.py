@@ -214,11 +214,11 @@ def dfa_debug_mma(form: int, A, B, C=None, stream=None):
 
 
 def dfa_debug_cta_trace(buf=None):
-    """Turns the per-CTA timeline on (buf: int64 CUDA tensor of 8*n records) or off (None)."""
+    """Turns the per-CTA timeline on (buf: int64 CUDA tensor of 16*n) or off (None)."""
     if buf is None:
         _check(_lib.dfa_debug_cta_trace(None, 0))
     else:
-        _check(_lib.dfa_debug_cta_trace(_ptr(buf), buf.numel() // 8))
+        _check(_lib.dfa_debug_cta_trace(_ptr(buf), buf.numel() // 16))
     return buf
 
 

@@ -19,7 +19,7 @@ def test_kernels_follow_the_work_list(shape, sched):
     q, k, v, do = make(B, H, Hkv, S, D, torch.bfloat16, seed=3, device="cuda")
     O, lse = dfa.dfa_attn_fwd(q, k, v, sched=sched)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    buf = torch.zeros(8 * 1024, dtype=torch.int64, device="cuda")
+    buf = torch.zeros(16 * 1024, dtype=torch.int64, device="cuda")
     for which in ("fwd", "bwd"):
         buf.zero_()
         dfa.dfa_debug_cta_trace(buf)
