@@ -1,0 +1,519 @@
+// bwd_pipe_tc.cu -- pipelined tcgen05 causal attention backward, head dim 128.
+//
+// Same mathematics and contract as bwd_tc.cu (DISTFLASHATTN §3.3, paperlayer.ai
+// summary of arXiv 2310.03294: the backward reads the saved output and
+// log-sum-exp and never re-runs the forward; P is recomputed from lse):
+//   dV_j += P_ij dO_i,  dS_ij = P_ij (dO_i . v_j - Delta_i),
+//   dK_j += dS_ij q_i,  dQ_i += dS_ij k_j           (scale applied at the end).
+//
+// What differs from bwd_tc.cu is the schedule.  The softmax-gradient work of
+// a (128-key x 128-query) tile is split into two phases:
+//   phase 1  P^T = exp2(S^T c - lse2)  -- needs S^T only; P^T goes to TMEM
+//            (bf16, over S^T) for dV and stays in registers (bf16 pairs);
+//   phase 2  dS^T = P^T (dP^T - Delta) -- needs dP^T; dS^T goes to swizzled
+//            shared memory for dK and dQ.
+// so the tensor cores can run dV(n) and S^T(n+1) as soon as phase 1 of tile n
+// is done, and the exponentials of tile n+1 overlap dK/dQ of tile n:
+//   MMA order per tile n:  [phase1(n)] dV(n), S^T(n+1)  [phase2(n)] dQ^T(n),
+//                          dK(n)  [drain(n)] dP^T(n+1)
+// (dQ^T before dK, so the drain reads dQ^T out of TMEM while dK runs).
+//   P/dS warps per tile:   phase1(n), phase2(n), phase1(n+1), ...
+// All MMAs are N = 128 or 128-row wide (few, large instructions: one thread
+// issues them all).  Two warpgroups split the 128 query columns (two warps
+// per SM sub-partition hide each other's latency); a third drains dQ.
+//
+// TMEM columns: dV [0,128) dK [128,256) S^T [256,384) (P^T of query half h at
+// [256+64h, 256+64h+32)), dP^T / dQ^T [384,512).
+// Roles (512 threads, one CTA per SM, persistent over the work list):
+// warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM owner, warps 4-11
+// P/dS (two warpgroups by query half) and the dK/dV epilogue, warps 12-15
+// dQ drain (dQ^T out of TMEM, fp32 atomic adds; a warp's adds cover 128
+// contiguous bytes of one dQ row).
+// Trace wait slots (cycles): 0 P/dS dP^T, 1 MMA inputs, 2 MMA dq_free,
+// 3 MMA P^T done, 4 MMA dS^T done, 5 P/dS Q + S^T, 6 P/dS accumulators, 7 drain.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dfa {
+namespace {
+
+using namespace ptx;
+
+constexpr int kThreads = 512;
+constexpr int BT = 128;          // key rows per work item; query rows per tile
+constexpr int D = 128;
+constexpr int kTile = BT * D * 2;                  // 32 KB bf16 tile
+constexpr int kSide = 1024;                        // lse2[128] + Delta[128] per query tile
+constexpr int kOffK = 0, kOffV = kTile, kOffQ = 2 * kTile, kOffDO = 4 * kTile, kOffDS = 6 * kTile;
+constexpr int kOffSide = kOffDS + 32768;
+constexpr int kOffBar = kOffSide + 2 * kSide;
+constexpr int kSmem = kOffBar + 256;
+static_assert(kSmem <= 232448, "shared memory");
+
+constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384;
+
+struct Args {
+    int B, H, Hkv, S, S_pad, causal;
+    float scale, c2;
+    const float* lse2;
+    const float* delta;
+    float* dq_acc;
+    __nv_bfloat16* dK;
+    __nv_bfloat16* dV;
+    const int32_t* wl_offsets;
+    const int32_t* wl_items;
+    int n_units;
+    int* err;
+    uint64_t* trace;
+    int trace_cap;
+};
+
+struct Item {
+    int b, g, t, i0, n_q, ntiles;   // ntiles: 128-row query tiles over all heads of the group
+};
+
+__device__ __forceinline__ Item decode(const Args& a, int it) {
+    Item x;
+    const int row = it / a.n_units, unit = it % a.n_units;
+    x.b = row / a.Hkv;
+    x.g = row % a.Hkv;
+    x.t = a.n_units - 1 - unit;
+    x.n_q = (a.S + BT - 1) / BT;
+    x.i0 = a.causal ? x.t : 0;
+    x.ntiles = (a.H / a.Hkv) * (x.n_q - x.i0);
+    return x;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO, const Args a) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    if (smem_u32(smem) & 1023u) {
+        if (threadIdx.x == 0 && a.err) atomicExch(a.err, 2);
+        return;
+    }
+    uint8_t* sK = smem + kOffK;
+    uint8_t* sV = smem + kOffV;
+    uint8_t* sQ = smem + kOffQ;
+    uint8_t* sdO = smem + kOffDO;
+    uint8_t* sdS = smem + kOffDS;
+    uint8_t* sSide = smem + kOffSide;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+    uint64_t* kv_full = bars + 0;
+    uint64_t* kv_empty = bars + 1;
+    uint64_t* q_full = bars + 2;      // [2] per tile slot
+    uint64_t* q_empty = bars + 4;     // [2]
+    uint64_t* do_full = bars + 6;     // [2]
+    uint64_t* do_empty = bars + 8;    // [2]
+    uint64_t* s_full = bars + 10;     // S^T of the tile ready
+    uint64_t* dp_full = bars + 11;    // dP^T of the tile ready
+    uint64_t* p_done = bars + 12;     // phase 1 done: P^T in TMEM, S^T columns read
+    uint64_t* ds_done = bars + 13;    // phase 2 done: dS^T in smem, dP^T columns read
+    uint64_t* dq_full = bars + 14;    // dQ^T ready
+    uint64_t* dq_free = bars + 15;    // dQ^T read out
+    uint64_t* kd_full = bars + 16;
+    uint64_t* kd_empty = bars + 17;
+    uint64_t* done = bars + 18;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 24);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 25);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int it_begin = a.wl_offsets[blockIdx.x], it_end = a.wl_offsets[blockIdx.x + 1];
+    const int G = a.H / a.Hkv;
+
+    if (threadIdx.x == 0) {
+        mbar_init(kv_full, 1);
+        mbar_init(kv_empty, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&q_full[s], 1);
+            mbar_init(&q_empty[s], 1);
+            mbar_init(&do_full[s], 1);
+            mbar_init(&do_empty[s], 1);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(dp_full, 1);
+        mbar_init(p_done, 2 * BT);
+        mbar_init(ds_done, 2 * BT);
+        mbar_init(dq_full, 1);
+        mbar_init(dq_free, BT);
+        mbar_init(kd_full, 1);
+        mbar_init(kd_empty, 2 * BT);
+        mbar_init(done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmdO);
+    }
+    if (warp == 2) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint64_t t_start = globaltimer();
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        uint32_t n = 0, kvi = 0, kv_issued = 0, q_issued = 0, do_issued = 0;
+        bool ok = true;
+        uint64_t wt = 0;
+        auto wait = [&](uint64_t* bar, uint32_t parity) {
+            ok = ok && __all_sync(0xffffffffu, mbar_wait_acc(bar, parity, abort_flag, a.err, a.trace ? &wt : nullptr));
+            return ok;
+        };
+        for (int it = it_begin; it < it_end && ok; ++it) {
+            const Item x = decode(a, a.wl_items[it]);
+            if (!wait(kv_empty, (kvi & 1) ^ 1)) break;
+            ++kv_issued;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(kv_full, 2 * kTile);
+                for (int blk = 0; blk < 2; ++blk) {
+                    tma_load_4d(sK + blk * 16384, &tmK, kv_full, blk * 64, x.g, x.t * BT, x.b);
+                    tma_load_4d(sV + blk * 16384, &tmV, kv_full, blk * 64, x.g, x.t * BT, x.b);
+                }
+            }
+            __syncwarp();
+            for (int k = 0; k < x.ntiles && ok; ++k, ++n) {
+                const int h = x.g * G + k / (x.n_q - x.i0), i = x.i0 + k % (x.n_q - x.i0);
+                const size_t side_off = ((size_t)x.b * a.H + h) * a.S_pad + (size_t)i * BT;
+                const uint32_t s = n & 1, ph = ((n >> 1) & 1) ^ 1;
+                if (!wait(&q_empty[s], ph)) break;
+                ++q_issued;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&q_full[s], kTile + kSide);
+                    for (int blk = 0; blk < 2; ++blk)
+                        tma_load_4d(sQ + s * kTile + blk * 16384, &tmQ, &q_full[s], blk * 64, h, i * BT, x.b);
+                    bulk_load(sSide + s * kSide, a.lse2 + side_off, 512, &q_full[s]);
+                    bulk_load(sSide + s * kSide + 512, a.delta + side_off, 512, &q_full[s]);
+                }
+                __syncwarp();
+                if (!wait(&do_empty[s], ph)) break;
+                ++do_issued;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&do_full[s], kTile);
+                    for (int blk = 0; blk < 2; ++blk)
+                        tma_load_4d(sdO + s * kTile + blk * 16384, &tmdO, &do_full[s], blk * 64, h, i * BT, x.b);
+                }
+                __syncwarp();
+            }
+            ++kvi;
+        }
+        if (!ok && lane == 0) {
+            int dummy = 0;
+            if (kv_issued) mbar_wait(kv_full, (kv_issued - 1) & 1, &dummy, nullptr);
+            for (uint32_t m = (q_issued >= 2 ? q_issued - 2 : 0); m < q_issued; ++m)
+                mbar_wait(&q_full[m & 1], (m >> 1) & 1, &dummy, nullptr);
+            for (uint32_t m = (do_issued >= 2 ? do_issued - 2 : 0); m < do_issued; ++m)
+                mbar_wait(&do_full[m & 1], (m >> 1) & 1, &dummy, nullptr);
+        }
+        if (lane == 0) {
+            trace_count(a.trace, a.trace_cap, 6, n);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        constexpr uint32_t idS = idesc_bf16_f32(BT, BT, false, false);   // S^T, dP^T
+        constexpr uint32_t idKM = idesc_bf16_f32(BT, D, false, true);    // dV, dK: B N-major
+        constexpr uint32_t idQ = idesc_bf16_f32(D, BT, true, true);      // dQ^T: M = head dim
+        const uint64_t dKk = sdesc_sw128(smem_u32(sK), 16, 1024), dKn = sdesc_sw128(smem_u32(sK), 16384, 1024);
+        const uint64_t dVk = sdesc_sw128(smem_u32(sV), 16, 1024);
+        const uint64_t dQk = sdesc_sw128(smem_u32(sQ), 16, 1024), dQn = sdesc_sw128(smem_u32(sQ), 16384, 1024);
+        const uint64_t dOk = sdesc_sw128(smem_u32(sdO), 16, 1024), dOn = sdesc_sw128(smem_u32(sdO), 16384, 1024);
+        const uint64_t dSk = sdesc_sw128(smem_u32(sdS), 16, 1024), dSn = sdesc_sw128(smem_u32(sdS), 16384, 1024);
+        constexpr uint64_t kSlot = kTile >> 4, kRows16 = 2048 >> 4;
+        auto kmaj = [](int kk) -> uint64_t { return (uint64_t)(((kk / 4) * 16384 + (kk % 4) * 32) >> 4); };
+        uint32_t n = 0, kvi = 0;
+        bool ok = true;
+        uint64_t wt[4] = {0, 0, 0, 0};   // inputs (Q, dO, K/V, dK/dV free), dq_free, P^T, dS^T
+        auto wait = [&](uint64_t* bar, uint32_t parity, int slot) {
+            ok = ok && __all_sync(0xffffffffu,
+                                  mbar_wait_acc(bar, parity, abort_flag, a.err, a.trace ? &wt[slot] : nullptr));
+            if (ok) tc_fence_after();
+            return ok;
+        };
+        auto commit = [&](uint64_t* bar) {
+            if (lane == 0) mma_commit(bar);
+            __syncwarp();
+        };
+        auto issue_S = [&](uint32_t m) {   // S^T(m) = K Q_m^T
+            const uint32_t s = m & 1;
+            if (!wait(&q_full[s], (m >> 1) & 1, 0)) return false;
+            if (lane == 0) {
+                const uint64_t b0 = dQk + s * kSlot;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + kColS, dKk + kmaj(kk), b0 + kmaj(kk), idS, kk > 0);
+            }
+            commit(s_full);
+            return true;
+        };
+        auto issue_dP = [&](uint32_t m) {  // dP^T(m) = V dO_m^T, over the drained dQ^T(m-1)
+            const uint32_t s = m & 1;
+            if (!wait(&do_full[s], (m >> 1) & 1, 0)) return false;
+            if (m > 0 && !wait(dq_free, (m - 1) & 1, 1)) return false;
+            if (lane == 0) {
+                const uint64_t b0 = dOk + s * kSlot;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + kColDP, dVk + kmaj(kk), b0 + kmaj(kk), idS, kk > 0);
+            }
+            commit(dp_full);
+            return true;
+        };
+        for (int it = it_begin; it < it_end && ok; ++it) {
+            const Item x = decode(a, a.wl_items[it]);
+            if (!wait(kv_full, kvi & 1, 0)) break;
+            if (!issue_S(n) || !issue_dP(n)) break;
+            for (int k = 0; k < x.ntiles && ok; ++k, ++n) {
+                const uint32_t s = n & 1;
+                const bool more = k + 1 < x.ntiles;
+                if (k == 0 && !wait(kd_empty, (kvi & 1) ^ 1, 0)) break;
+                if (!wait(p_done, n & 1, 2)) break;
+                const uint32_t acc0 = k > 0 ? 1u : 0u;
+                if (lane == 0) {   // dV += P^T dO: P^T of query half h at S + 64h
+                    const uint64_t b0 = dOn + s * kSlot;
+#pragma unroll
+                    for (int kk = 0; kk < BT / 16; ++kk)
+                        mma_ts(tmem + kColDV, tmem + kColS + kk * 8 + (kk >= 4 ? 32 : 0), b0 + kk * kRows16, idKM,
+                               kk > 0 ? 1u : acc0);
+                }
+                commit(&do_empty[s]);
+                if (more && !issue_S(n + 1)) break;       // S^T columns are free after phase 1
+                if (!wait(ds_done, n & 1, 3)) break;
+                if (lane == 0) {   // dQ^T = K^T dS^T into the dP^T columns; drained while dK runs
+#pragma unroll
+                    for (int kk = 0; kk < BT / 16; ++kk)
+                        mma_ss(tmem + kColDP, dKn + kk * kRows16, dSn + kk * kRows16, idQ, kk > 0);
+                }
+                commit(dq_full);
+                if (lane == 0) {   // dK += dS^T Q
+                    const uint64_t bq = dQn + s * kSlot;
+#pragma unroll
+                    for (int kk = 0; kk < BT / 16; ++kk)
+                        mma_ss(tmem + kColDK, dSk + kmaj(kk), bq + kk * kRows16, idKM, kk > 0 ? 1u : acc0);
+                }
+                commit(&q_empty[s]);
+                if (!more) {
+                    commit(kd_full);
+                    commit(kv_empty);
+                } else if (!issue_dP(n + 1)) {
+                    break;
+                }
+            }
+            if (!ok) break;
+            ++kvi;
+        }
+        commit(done);
+        int dummy = 0;
+        mbar_wait(done, 0, &dummy, a.err);
+        if (lane == 0) {
+            trace_count(a.trace, a.trace_cap, 4, n);
+            for (int z = 0; z < 4; ++z) trace_wait(a.trace, a.trace_cap, 1 + z, wt[z]);
+        }
+    } else if (warp >= 4 && warp < 12) {
+        // ------------------------------------------------------------ P^T / dS^T, dK/dV epilogue
+        const int half = (warp - 4) / 4;                   // query columns [64 half, 64 half + 64)
+        const int r = (warp % 4) * 32 + lane;              // key row == TMEM lane
+        const uint32_t lane_base = (uint32_t)((warp % 4) * 32) << 16;
+        const uint32_t tS = tmem + lane_base + kColS + half * 64;
+        const uint32_t tdP = tmem + lane_base + kColDP + half * 64;
+        uint8_t* blk = sdS + half * 16384;
+        uint32_t n = 0, kvi = 0;
+        bool ok = true;
+        uint64_t wt[3] = {0, 0, 0};   // Q/S^T, dK/dV accumulators, dP^T
+        auto wait = [&](uint64_t* bar, uint32_t parity, int slot) {
+            ok = ok && __all_sync(0xffffffffu,
+                                  mbar_wait_acc(bar, parity, abort_flag, a.err, a.trace ? &wt[slot] : nullptr));
+            return ok;
+        };
+        for (int it = it_begin; it < it_end && ok; ++it) {
+            const Item x = decode(a, a.wl_items[it]);
+            const int kvg = x.t * BT + r;
+            const bool row_ok = kvg < a.S;
+            for (int k = 0; k < x.ntiles; ++k, ++n) {
+                const int i = x.i0 + k % (x.n_q - x.i0);
+                const uint32_t s = n & 1;
+                const int q0 = i * BT + half * 64;
+                if (!wait(&q_full[s], (n >> 1) & 1, 0) || !wait(s_full, n & 1, 0)) break;
+                tc_fence_after();
+                const float* lse2 = reinterpret_cast<const float*>(sSide + s * kSide) + half * 64;
+                const float* dl = lse2 + BT;
+                // ---- phase 1: P^T = exp2(S^T c - lse2) -> TMEM (bf16) and registers
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t us[32];
+                    tmem_ld32(tS + c * 32, us);
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4) {
+                        const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c * 32 + e);
+                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+                        float pp[4];
+#pragma unroll
+                        for (int z = 0; z < 4; ++z) {
+                            const int qg = q0 + c * 32 + e + z;
+                            const bool vis = row_ok && qg < a.S && !(a.causal && kvg > qg);
+                            pp[z] = vis ? ex2(fmaf(__uint_as_float(us[e + z]), a.c2, -lv[z])) : 0.f;
+                        }
+                        pk[c * 16 + e / 2] = pack_bf16(pp[0], pp[1]);
+                        pk[c * 16 + e / 2 + 1] = pack_bf16(pp[2], pp[3]);
+                    }
+                    tmem_st16(tS + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[c * 16]));
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(p_done);
+                // ---- phase 2: dS^T = P^T (dP^T - Delta) -> swizzled smem (bf16)
+                if (!wait(dp_full, n & 1, 2)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t ud[32];
+                    tmem_ld32(tdP + c * 32, ud);
+                    uint32_t dk[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4) {
+                        const float4 d4 = *reinterpret_cast<const float4*>(dl + c * 32 + e);
+                        const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+                        const float2 p01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[c * 16 + e / 2]));
+                        const float2 p23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[c * 16 + e / 2 + 1]));
+                        const float pp[4] = {p01.x, p01.y, p23.x, p23.y};
+                        float dd[4];
+#pragma unroll
+                        for (int z = 0; z < 4; ++z) dd[z] = pp[z] * (__uint_as_float(ud[e + z]) - dv[z]);
+                        dk[e / 2] = pack_bf16(dd[0], dd[1]);
+                        dk[e / 2 + 1] = pack_bf16(dd[2], dd[3]);
+                    }
+#pragma unroll
+                    for (int z = 0; z < 4; ++z)
+                        *reinterpret_cast<uint4*>(blk + sw128_offset(r, c * 32 + z * 8)) =
+                            make_uint4(dk[4 * z], dk[4 * z + 1], dk[4 * z + 2], dk[4 * z + 3]);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(ds_done);
+            }
+            if (!ok) break;
+            // ---- epilogue: dV = acc, dK = scale * acc, bf16 [B, S, Hkv, D]; this half's columns
+            if (!wait(kd_full, kvi & 1, 1)) break;
+            tc_fence_after();
+            const int64_t orow = (((int64_t)x.b * a.S + kvg) * a.Hkv + x.g) * D;
+#pragma unroll 1
+            for (int c = half * 2; c < half * 2 + 2; ++c) {
+                uint32_t uv[32], uk[32];
+                tmem_ld32x2(tmem + lane_base + kColDV + c * 32, tmem + lane_base + kColDK + c * 32, uv, uk);
+                if (row_ok) {
+                    uint4* pv = reinterpret_cast<uint4*>(a.dV + orow + c * 32);
+                    uint4* pkk = reinterpret_cast<uint4*>(a.dK + orow + c * 32);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        uint4 v, w;
+                        v.x = pack_bf16(__uint_as_float(uv[8 * e + 0]), __uint_as_float(uv[8 * e + 1]));
+                        v.y = pack_bf16(__uint_as_float(uv[8 * e + 2]), __uint_as_float(uv[8 * e + 3]));
+                        v.z = pack_bf16(__uint_as_float(uv[8 * e + 4]), __uint_as_float(uv[8 * e + 5]));
+                        v.w = pack_bf16(__uint_as_float(uv[8 * e + 6]), __uint_as_float(uv[8 * e + 7]));
+                        w.x = pack_bf16(a.scale * __uint_as_float(uk[8 * e + 0]), a.scale * __uint_as_float(uk[8 * e + 1]));
+                        w.y = pack_bf16(a.scale * __uint_as_float(uk[8 * e + 2]), a.scale * __uint_as_float(uk[8 * e + 3]));
+                        w.z = pack_bf16(a.scale * __uint_as_float(uk[8 * e + 4]), a.scale * __uint_as_float(uk[8 * e + 5]));
+                        w.w = pack_bf16(a.scale * __uint_as_float(uk[8 * e + 6]), a.scale * __uint_as_float(uk[8 * e + 7]));
+                        pv[e] = v;
+                        pkk[e] = w;
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(kd_empty);
+            ++kvi;
+        }
+        if (threadIdx.x == 128) {
+            trace_count(a.trace, a.trace_cap, 5, n);
+            trace_wait(a.trace, a.trace_cap, 5, wt[0]);
+            trace_wait(a.trace, a.trace_cap, 6, wt[1]);
+            trace_wait(a.trace, a.trace_cap, 0, wt[2]);
+        }
+    } else if (warp >= 12) {
+        // ------------------------------------------------------------ dQ drain
+        // TMEM lane r = head-dim element r of dQ^T; column c = query row i*128 + c.
+        const int r = (warp % 4) * 32 + lane;
+        const uint32_t tdQ = tmem + ((uint32_t)((warp % 4) * 32) << 16) + kColDP;
+        uint32_t n = 0;
+        bool ok = true;
+        uint64_t wt = 0;
+        for (int it = it_begin; it < it_end && ok; ++it) {
+            const Item x = decode(a, a.wl_items[it]);
+            for (int k = 0; k < x.ntiles; ++k, ++n) {
+                const int h = x.g * G + k / (x.n_q - x.i0), i = x.i0 + k % (x.n_q - x.i0);
+                ok = __all_sync(0xffffffffu, mbar_wait_acc(dq_full, n & 1, abort_flag, a.err, a.trace ? &wt : nullptr));
+                if (!ok) break;
+                tc_fence_after();
+                float* base = a.dq_acc + ((int64_t)x.b * a.S + (int64_t)i * BT) * a.H * D + (int64_t)h * D + r;
+                const int64_t stride = (int64_t)a.H * D;
+                const int nq = min(BT, a.S - i * BT);
+                // Two halves of 64 query columns (64 registers each); TMEM is
+                // released once the second half has been read.
+#pragma unroll 1
+                for (int hf = 0; hf < 2; ++hf) {
+                    uint32_t v0[32], v1[32];
+                    tmem_ld32x2(tdQ + hf * 64, tdQ + hf * 64 + 32, v0, v1);
+                    if (hf == 1) {
+                        tc_fence_before();
+                        mbar_arrive(dq_free);
+                    }
+                    float* bh = base + (int64_t)(hf * 64) * stride;
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        if (hf * 64 + c < nq) atomicAdd(bh + c * stride, __uint_as_float(v0[c]));
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        if (hf * 64 + 32 + c < nq) atomicAdd(bh + (32 + c) * stride, __uint_as_float(v1[c]));
+                }
+            }
+        }
+        if (threadIdx.x == 384) {
+            trace_count(a.trace, a.trace_cap, 7, n);
+            trace_wait(a.trace, a.trace_cap, 7, wt);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 2) tmem_dealloc(tmem, 512);
+    if (threadIdx.x == 0) trace_cta(a.trace, a.trace_cap, t_start, it_end - it_begin);
+}
+
+}  // namespace
+
+dfa_status tc_bwd_pipelined(const AttnProblem& p, const void* q, const void* k, const void* v, const void* dO,
+                            const float* lse2, const float* delta, int S_pad, float* dq_acc, void* dK, void* dV,
+                            const WorkList* wl, cudaStream_t s) {
+    if (p.D != D) return fail(DFA_ERR_UNSUPPORTED, "pipelined backward needs D = 128");
+    alignas(64) CUtensorMap mq, mk, mv, mdo;
+    if (!make_tmap_bshd(&mq, q, p.B, p.Lq, p.H, D, p.q_sb, p.q_ss, p.q_sh) ||
+        !make_tmap_bshd(&mdo, dO, p.B, p.Lq, p.H, D, p.q_sb, p.q_ss, p.q_sh) ||
+        !make_tmap_bshd(&mk, k, p.B, p.Lkv, p.Hkv, D, p.kv_sb, p.kv_ss, p.kv_sh) ||
+        !make_tmap_bshd(&mv, v, p.B, p.Lkv, p.Hkv, D, p.kv_sb, p.kv_ss, p.kv_sh))
+        return fail(DFA_ERR_CUDA, "tensor map encoding failed");
+    Args a{};
+    a.B = p.B; a.H = p.H; a.Hkv = p.Hkv; a.S = p.Lq; a.S_pad = S_pad; a.causal = p.causal;
+    a.scale = p.scale; a.c2 = p.scale * 1.4426950408889634f;
+    a.lse2 = lse2; a.delta = delta; a.dq_acc = dq_acc;
+    a.dK = static_cast<__nv_bfloat16*>(dK);
+    a.dV = static_cast<__nv_bfloat16*>(dV);
+    a.wl_offsets = wl->offsets; a.wl_items = wl->items; a.n_units = wl->n_units;
+    a.err = device_error_flag();
+    a.trace = cta_trace(&a.trace_cap);
+    if (cudaFuncSetAttribute(bwd_pipe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
+        return fail(DFA_ERR_CUDA, "bwd_pipe: shared memory attribute");
+    bwd_pipe_kernel<<<wl->n_workers, kThreads, kSmem, s>>>(mq, mk, mv, mdo, a);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? DFA_OK : fail(DFA_ERR_CUDA, "bwd_pipe launch: %s", cudaGetErrorString(e));
+}
+
+}  // namespace dfa

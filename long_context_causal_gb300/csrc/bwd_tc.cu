@@ -518,8 +518,9 @@ dfa_status tc_bwd(const AttnProblem& p, const void* q, const void* k, const void
                   const float* lse2, const float* delta, int S_pad, float* dq_acc, void* dK, void* dV,
                   const WorkList* wl, cudaStream_t s) {
     if (p.B == 0 || p.Lq == 0) return DFA_OK;
-    return p.D == 128 ? launch<128>(p, q, k, v, dO, lse2, delta, S_pad, dq_acc, dK, dV, wl, s)
-                      : launch<64>(p, q, k, v, dO, lse2, delta, S_pad, dq_acc, dK, dV, wl, s);
+    // Head dim 128 takes the two-stream pipelined kernel (bwd_pipe_tc.cu).
+    if (p.D == 128) return tc_bwd_pipelined(p, q, k, v, dO, lse2, delta, S_pad, dq_acc, dK, dV, wl, s);
+    return launch<64>(p, q, k, v, dO, lse2, delta, S_pad, dq_acc, dK, dV, wl, s);
 }
 
 }  // namespace dfa

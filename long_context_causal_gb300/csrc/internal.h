@@ -65,6 +65,12 @@ dfa_status tc_bwd(const AttnProblem& p, const void* q, const void* k, const void
                   const void* dO, const float* lse2, const float* delta, int S_pad, float* dq_acc,
                   void* dK, void* dV, const WorkList* wl, cudaStream_t s);
 
+// Head-dim-128 backward with the softmax-gradient split into two phases so the
+// tensor cores overlap it (bwd_pipe_tc.cu).
+dfa_status tc_bwd_pipelined(const AttnProblem& p, const void* q, const void* k, const void* v,
+                            const void* dO, const float* lse2, const float* delta, int S_pad,
+                            float* dq_acc, void* dK, void* dV, const WorkList* wl, cudaStream_t s);
+
 int num_sms();
 
 // 4-D bf16 TMA descriptor over a [B, L, heads, D] tensor (element strides sb,
