@@ -7,7 +7,8 @@
 //  * delta:   Delta_i = <dO_i, O_i>, the per-row term of the softmax gradient,
 //             read once from the SAVED output (§3.3: the backward reuses the
 //             forward's output instead of recomputing it);
-//  * convert: the fp32 dQ accumulator scaled and cast to the output dtype.
+//  * convert: the head-major fp32 dQ accumulator [B, H, S, D] scaled, cast to the
+//    output dtype and written as [B, S, H, D].
 // Each is a streaming pass: one warp per row, 16-byte loads, no reuse.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -133,12 +134,24 @@ bwd_prep_kernel(int B, int H, int S, int S_pad, int D, const T* __restrict__ O, 
     }
 }
 
-__global__ void convert_bf16_kernel(int64_t n, float scale, const float* __restrict__ in,
+// Eight consecutive head-dim elements per thread: output x*8 of [B, S, H, D]
+// comes from the head-major accumulator [B, H, S, D].
+__device__ __forceinline__ int64_t acc_index(int64_t o, int H, int S, int D) {
+    const int d = (int)(o % D);
+    const int64_t r = o / D;
+    const int h = (int)(r % H);
+    const int64_t bs = r / H;
+    const int s = (int)(bs % S);
+    const int64_t b = bs / S;
+    return ((b * H + h) * S + s) * D + d;
+}
+
+__global__ void convert_bf16_kernel(int64_t n, int H, int S, int D, float scale, const float* __restrict__ in,
                                     __nv_bfloat16* __restrict__ out) {
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < n / 8; x += stride) {
-        const float4 a = reinterpret_cast<const float4*>(in)[2 * x];
-        const float4 b = reinterpret_cast<const float4*>(in)[2 * x + 1];
+        const float4* src = reinterpret_cast<const float4*>(in + acc_index(8 * x, H, S, D));
+        const float4 a = src[0], b = src[1];
         __nv_bfloat162 r[4] = {__floats2bfloat162_rn(scale * a.x, scale * a.y),
                                __floats2bfloat162_rn(scale * a.z, scale * a.w),
                                __floats2bfloat162_rn(scale * b.x, scale * b.y),
@@ -147,11 +160,16 @@ __global__ void convert_bf16_kernel(int64_t n, float scale, const float* __restr
     }
 }
 
-__global__ void convert_f32_kernel(int64_t n, float scale, const float* __restrict__ in,
+__global__ void convert_f32_kernel(int64_t n, int H, int S, int D, float scale, const float* __restrict__ in,
                                    float* __restrict__ out) {
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < n; x += stride)
-        out[x] = scale * in[x];
+    for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < n / 8; x += stride) {
+        const float4* src = reinterpret_cast<const float4*>(in + acc_index(8 * x, H, S, D));
+        const float4 a = src[0], b = src[1];
+        float4* dst = reinterpret_cast<float4*>(out) + 2 * x;
+        dst[0] = make_float4(scale * a.x, scale * a.y, scale * a.z, scale * a.w);
+        dst[1] = make_float4(scale * b.x, scale * b.y, scale * b.z, scale * b.w);
+    }
 }
 
 dfa_status launched(const char* what) {
@@ -198,14 +216,15 @@ dfa_status launch_bwd_prep(dfa_dtype dt, int B, int H, int S, int S_pad, int D, 
     return launched("bwd prep");
 }
 
-dfa_status launch_convert(dfa_dtype dt, int64_t n, float scale, const float* acc, void* out,
+dfa_status launch_convert(dfa_dtype dt, int B, int H, int S, int D, float scale, const float* acc, void* out,
                           cudaStream_t s) {
+    const int64_t n = (int64_t)B * S * H * D;
     if (n == 0) return DFA_OK;
     const int blocks = 8 * num_sms();
     if (dt == DFA_BF16)
-        convert_bf16_kernel<<<blocks, kThreads, 0, s>>>(n, scale, acc, (__nv_bfloat16*)out);
+        convert_bf16_kernel<<<blocks, kThreads, 0, s>>>(n, H, S, D, scale, acc, (__nv_bfloat16*)out);
     else
-        convert_f32_kernel<<<blocks, kThreads, 0, s>>>(n, scale, acc, (float*)out);
+        convert_f32_kernel<<<blocks, kThreads, 0, s>>>(n, H, S, D, scale, acc, (float*)out);
     return launched("convert");
 }
 

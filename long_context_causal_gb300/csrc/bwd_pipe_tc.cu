@@ -63,7 +63,7 @@ struct Args {
     float scale, c2;
     const float* lse2;
     const float* delta;
-    float* dq_acc;
+    float* dq_acc;                // [B, H, S, D] fp32, zeroed by the caller
     __nv_bfloat16* dK;
     __nv_bfloat16* dV;
     const int32_t* wl_offsets;
@@ -453,8 +453,9 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 ok = __all_sync(0xffffffffu, mbar_wait_acc(dq_full, n & 1, abort_flag, a.err, a.trace ? &wt : nullptr));
                 if (!ok) break;
                 tc_fence_after();
-                float* base = a.dq_acc + ((int64_t)x.b * a.S + (int64_t)i * BT) * a.H * D + (int64_t)h * D + r;
-                const int64_t stride = (int64_t)a.H * D;
+                // dQ accumulator is head-major [B, H, S, D]: the tile is one contiguous 64 KB block.
+                float* base = a.dq_acc + (((int64_t)x.b * a.H + h) * a.S + (int64_t)i * BT) * D + r;
+                constexpr int64_t stride = D;
                 const int nq = min(BT, a.S - i * BT);
                 // Two halves of 64 query columns (64 registers each); TMEM is
                 // released once the second half has been read.
@@ -462,9 +463,9 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 for (int hf = 0; hf < 2; ++hf) {
                     uint32_t v0[32], v1[32];
                     tmem_ld32x2(tdQ + hf * 64, tdQ + hf * 64 + 32, v0, v1);
-                    if (hf == 1) {
+                    if (hf == 1) {   // relaxed: the arrival must not wait for the first half's adds
                         tc_fence_before();
-                        mbar_arrive(dq_free);
+                        mbar_arrive_relaxed(dq_free);
                     }
                     float* bh = base + (int64_t)(hf * 64) * stride;
 #pragma unroll

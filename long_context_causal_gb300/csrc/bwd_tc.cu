@@ -67,7 +67,7 @@ struct BwdArgs {
     float scale, c2;              // c2 = scale * log2(e)
     const float* lse2;            // [B, H, S_pad]  lse * log2(e)
     const float* delta;           // [B, H, S_pad]
-    float* dq_acc;                // [B, S, H, D] fp32, zeroed by the caller
+    float* dq_acc;                // [B, H, S, D] fp32, zeroed by the caller
     __nv_bfloat16* dK;            // [B, S, Hkv, D]
     __nv_bfloat16* dV;
     const int32_t* wl_offsets;
@@ -455,15 +455,15 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 mbar_arrive(dq_free);
                 if constexpr (D == 128) {
                     // Column c is query row i*128 + c: the warp adds 32 consecutive floats of it.
-                    float* base = a.dq_acc + ((int64_t)x.b * a.S + (int64_t)i * BT) * a.H * D + (int64_t)h * D + r;
+                    float* base = a.dq_acc + (((int64_t)x.b * a.H + h) * a.S + (int64_t)i * BT) * D + r;
                     const int nq = min(BT, a.S - i * BT);
 #pragma unroll
                     for (int c = 0; c < BT; ++c)
-                        if (c < nq) atomicAdd(base + (int64_t)c * a.H * D, __uint_as_float(u[c]));
+                        if (c < nq) atomicAdd(base + (int64_t)c * D, __uint_as_float(u[c]));
                 } else {
                     const int qg = i * BT + r;
                     if (qg < a.S) {
-                        float4* dst = reinterpret_cast<float4*>(a.dq_acc + (((int64_t)x.b * a.S + qg) * a.H + h) * D);
+                        float4* dst = reinterpret_cast<float4*>(a.dq_acc + (((int64_t)x.b * a.H + h) * a.S + qg) * D);
 #pragma unroll
                         for (int e = 0; e < D / 4; ++e)
                             atomicAdd(dst + e, make_float4(__uint_as_float(u[4 * e]), __uint_as_float(u[4 * e + 1]),

@@ -334,7 +334,7 @@ extern "C" dfa_status dfa_attn_bwd(const void* q, const void* k, const void* v, 
     WorkList wl{dev, dev + workers + 1, workers, units};
     if ((st = tc_bwd(p, q, k, v, dO, lse2, delta, L.S_pad, dq_acc, dK, dV, &wl, s))) return st;
     count_launch(DFA_KERNEL_BWD);
-    st = launch_convert(dt, (int64_t)B * S * H * D, scale, dq_acc, dQ, s);
+    st = launch_convert(dt, B, H, S, D, scale, dq_acc, dQ, s);
     if (st == DFA_OK) count_launch(DFA_KERNEL_CONVERT);
     return st;
 }

@@ -46,8 +46,9 @@ dfa_status launch_delta(dfa_dtype dt, int B, int H, int S, int D, const void* O,
 // Delta = rowsum(dO * O), both written to [B, H, S_pad] with zero padding.
 dfa_status launch_bwd_prep(dfa_dtype dt, int B, int H, int S, int S_pad, int D, const void* O,
                            const void* dO, const float* lse, float* lse2, float* delta, cudaStream_t s);
-// out[x] = scale * acc[x] cast to dt, n elements.
-dfa_status launch_convert(dfa_dtype dt, int64_t n, float scale, const float* acc, void* out,
+// out[b, s, h, :] = scale * acc[b, h, s, :] cast to dt (acc is the head-major
+// fp32 dQ accumulator of the tensor-core backward; D a multiple of 8).
+dfa_status launch_convert(dfa_dtype dt, int B, int H, int S, int D, float scale, const float* acc, void* out,
                           cudaStream_t s);
 
 // ---- tcgen05 tensor-core kernels (fwd_tc.cu, bwd_tc.cu) ----
