@@ -47,6 +47,13 @@ def parse():
     return ap.parse_args()
 
 
+# DRAM bytes (read + write) per launch of the backward kernel, from one
+# single-pass ncu capture of this command's workload (profiles/
+# launches_llama7b_s128k.md).  Only valid for the kernel build it was taken on;
+# other workloads report null.
+NCU_BWD_TRAFFIC = {"llama7b_s128k": 109.61e9}
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -336,7 +343,8 @@ def main():
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
         "roofline": {"bound": "tensor", "kernel": "dfa_attn_bwd (delta + bwd + dQ convert)",
                      "achieved": bwd_tflops, "peak": peak_tc, "unit": "TFLOP/s",
-                     "frac": bwd_tflops / peak_tc, "traffic": None,
+                     "frac": bwd_tflops / peak_tc,
+                     "traffic": NCU_BWD_TRAFFIC.get(w.name) if args.shape is None else None,
                      "peak_kind": f"{peak_kind} bf16 burst"},
         "roofline_fwd": {"bound": "tensor", "achieved": fwd_tflops, "peak": peak_tc, "unit": "TFLOP/s",
                          "frac": fwd_tflops / peak_tc},
