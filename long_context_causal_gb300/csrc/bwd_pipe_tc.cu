@@ -27,8 +27,8 @@
 // Roles (512 threads, one CTA per SM, persistent over the work list):
 // warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM owner, warps 4-11
 // P/dS (two warpgroups by query half) and the dK/dV epilogue, warps 12-15
-// dQ drain (dQ^T out of TMEM, fp32 atomic adds; a warp's adds cover 128
-// contiguous bytes of one dQ row).
+// dQ drain (dQ^T out of TMEM, 16-byte fp32 reductions; a warp instruction
+// covers four full 128-byte dQ rows).
 // Trace wait slots (cycles): 0 P/dS dP^T, 1 MMA inputs, 2 MMA dq_free,
 // 3 MMA P^T done, 4 MMA dS^T done, 5 P/dS Q + S^T, 6 P/dS accumulators, 7 drain.
 #include <cuda.h>
@@ -74,8 +74,23 @@ struct Args {
     int trace_cap;
 };
 
+// Query tiles of an item are swept upwards for key tiles in the lower half of
+// the sequence and downwards for the upper half.  The balanced list gives a
+// worker a key tile t and then its mirror n-1-t; sweeping both upwards would
+// bring every worker's second item onto the same query tile at the same time
+// (all of them end at the last tile), and their fp32 dQ reductions would then
+// serialise on the same lines.  With the mirror swept downwards, workers stay
+// on distinct tiles of a window of about 150 tiles.  Any order is correct:
+// dK/dV accumulate and the dQ reductions commute.
 struct Item {
     int b, g, t, i0, n_q, ntiles;   // ntiles: 128-row query tiles over all heads of the group
+    bool down;                      // sweep query tiles from the last one down
+    // k-th tile of the item: head h of the group, query tile i
+    __device__ __forceinline__ void tile(int k, int G, int& h, int& i) const {
+        const int len = n_q - i0, r = k % len;
+        h = g * G + k / len;
+        i = down ? n_q - 1 - r : i0 + r;
+    }
 };
 
 __device__ __forceinline__ Item decode(const Args& a, int it) {
@@ -87,6 +102,7 @@ __device__ __forceinline__ Item decode(const Args& a, int it) {
     x.n_q = (a.S + BT - 1) / BT;
     x.i0 = a.causal ? x.t : 0;
     x.ntiles = (a.H / a.Hkv) * (x.n_q - x.i0);
+    x.down = 2 * x.t >= a.n_units;
     return x;
 }
 
@@ -184,7 +200,8 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             }
             __syncwarp();
             for (int k = 0; k < x.ntiles && ok; ++k, ++n) {
-                const int h = x.g * G + k / (x.n_q - x.i0), i = x.i0 + k % (x.n_q - x.i0);
+                int h, i;
+                x.tile(k, G, h, i);
                 const size_t side_off = ((size_t)x.b * a.H + h) * a.S_pad + (size_t)i * BT;
                 const uint32_t s = n & 1, ph = ((n >> 1) & 1) ^ 1;
                 if (!wait(&q_empty[s], ph)) break;
@@ -338,34 +355,39 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const int kvg = x.t * BT + r;
             const bool row_ok = kvg < a.S;
             for (int k = 0; k < x.ntiles; ++k, ++n) {
-                const int i = x.i0 + k % (x.n_q - x.i0);
+                int h, i;
+                x.tile(k, G, h, i);
+                (void)h;
                 const uint32_t s = n & 1;
                 const int q0 = i * BT + half * 64;
                 if (!wait(&q_full[s], (n >> 1) & 1, 0) || !wait(s_full, n & 1, 0)) break;
                 tc_fence_after();
                 const float* lse2 = reinterpret_cast<const float*>(sSide + s * kSide) + half * 64;
                 const float* dl = lse2 + BT;
+                // Elements outside the causal triangle or the sequence only occur on
+                // the diagonal tile and on ragged edges; elsewhere no mask is applied.
+                const bool full = !(a.causal && i == x.t) && (i + 1) * BT <= a.S && (x.t + 1) * BT <= a.S;
                 // ---- phase 1: P^T = exp2(S^T c - lse2) -> TMEM (bf16) and registers
-                uint32_t pk[32];
+                uint32_t u[32], pk[32];
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t us[32];
-                    tmem_ld32(tS + c * 32, us);
+                for (int c = 0; c < 64; c += 32) {
+                    tmem_ld32(tS + c, u);
+                    if (!full) {   // masked scores become -inf, so exp2 gives exactly 0
+#pragma unroll
+                        for (int z = 0; z < 32; ++z) {
+                            const int qg = q0 + c + z;
+                            if (!(row_ok && qg < a.S && !(a.causal && kvg > qg))) u[z] = 0xff800000u;
+                        }
+                    }
 #pragma unroll
                     for (int e = 0; e < 32; e += 4) {
-                        const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c * 32 + e);
-                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-                        float pp[4];
-#pragma unroll
-                        for (int z = 0; z < 4; ++z) {
-                            const int qg = q0 + c * 32 + e + z;
-                            const bool vis = row_ok && qg < a.S && !(a.causal && kvg > qg);
-                            pp[z] = vis ? ex2(fmaf(__uint_as_float(us[e + z]), a.c2, -lv[z])) : 0.f;
-                        }
-                        pk[c * 16 + e / 2] = pack_bf16(pp[0], pp[1]);
-                        pk[c * 16 + e / 2 + 1] = pack_bf16(pp[2], pp[3]);
+                        const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c + e);
+                        pk[(c + e) / 2] = pack_bf16(ex2(fmaf(__uint_as_float(u[e]), a.c2, -l4.x)),
+                                                    ex2(fmaf(__uint_as_float(u[e + 1]), a.c2, -l4.y)));
+                        pk[(c + e) / 2 + 1] = pack_bf16(ex2(fmaf(__uint_as_float(u[e + 2]), a.c2, -l4.z)),
+                                                        ex2(fmaf(__uint_as_float(u[e + 3]), a.c2, -l4.w)));
                     }
-                    tmem_st16(tS + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[c * 16]));
+                    tmem_st16(tS + c / 2, *reinterpret_cast<uint32_t(*)[16]>(&pk[c / 2]));
                 }
                 tmem_st_wait();
                 tc_fence_before();
@@ -374,27 +396,25 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 if (!wait(dp_full, n & 1, 2)) break;
                 tc_fence_after();
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t ud[32];
-                    tmem_ld32(tdP + c * 32, ud);
-                    uint32_t dk[16];
+                for (int c = 0; c < 64; c += 32) {
+                    tmem_ld32(tdP + c, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        const float4 d4 = *reinterpret_cast<const float4*>(dl + c * 32 + e);
-                        const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-                        const float2 p01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[c * 16 + e / 2]));
-                        const float2 p23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[c * 16 + e / 2 + 1]));
-                        const float pp[4] = {p01.x, p01.y, p23.x, p23.y};
-                        float dd[4];
+                    for (int e = 0; e < 32; e += 8) {
+                        uint32_t dk[4];
 #pragma unroll
-                        for (int z = 0; z < 4; ++z) dd[z] = pp[z] * (__uint_as_float(ud[e + z]) - dv[z]);
-                        dk[e / 2] = pack_bf16(dd[0], dd[1]);
-                        dk[e / 2 + 1] = pack_bf16(dd[2], dd[3]);
+                        for (int w = 0; w < 8; w += 4) {
+                            const float4 d4 = *reinterpret_cast<const float4*>(dl + c + e + w);
+                            const float2 p01 =
+                                __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[(c + e + w) / 2]));
+                            const float2 p23 =
+                                __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[(c + e + w) / 2 + 1]));
+                            dk[w / 2] = pack_bf16(p01.x * (__uint_as_float(u[e + w]) - d4.x),
+                                                  p01.y * (__uint_as_float(u[e + w + 1]) - d4.y));
+                            dk[w / 2 + 1] = pack_bf16(p23.x * (__uint_as_float(u[e + w + 2]) - d4.z),
+                                                      p23.y * (__uint_as_float(u[e + w + 3]) - d4.w));
+                        }
+                        *reinterpret_cast<uint4*>(blk + sw128_offset(r, c + e)) = make_uint4(dk[0], dk[1], dk[2], dk[3]);
                     }
-#pragma unroll
-                    for (int z = 0; z < 4; ++z)
-                        *reinterpret_cast<uint4*>(blk + sw128_offset(r, c * 32 + z * 8)) =
-                            make_uint4(dk[4 * z], dk[4 * z + 1], dk[4 * z + 2], dk[4 * z + 3]);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -440,8 +460,7 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
     } else if (warp >= 12) {
         // ------------------------------------------------------------ dQ drain
-        // TMEM lane r = head-dim element r of dQ^T; column c = query row i*128 + c.
-        const int r = (warp % 4) * 32 + lane;
+        // TMEM lane = head-dim element of dQ^T; column c = query row i*128 + c.
         const uint32_t tdQ = tmem + ((uint32_t)((warp % 4) * 32) << 16) + kColDP;
         uint32_t n = 0;
         bool ok = true;
@@ -449,31 +468,39 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         for (int it = it_begin; it < it_end && ok; ++it) {
             const Item x = decode(a, a.wl_items[it]);
             for (int k = 0; k < x.ntiles; ++k, ++n) {
-                const int h = x.g * G + k / (x.n_q - x.i0), i = x.i0 + k % (x.n_q - x.i0);
+                int h, i;
+                x.tile(k, G, h, i);
                 ok = __all_sync(0xffffffffu, mbar_wait_acc(dq_full, n & 1, abort_flag, a.err, a.trace ? &wt : nullptr));
                 if (!ok) break;
                 tc_fence_after();
-                // dQ accumulator is head-major [B, H, S, D]: the tile is one contiguous 64 KB block.
-                float* base = a.dq_acc + (((int64_t)x.b * a.H + h) * a.S + (int64_t)i * BT) * D + r;
-                constexpr int64_t stride = D;
+                // dQ accumulator is head-major [B, H, S, D]: the tile is one contiguous
+                // 64 KB block.  Each group of four query columns is transposed inside
+                // lane quads, so lane 4q+m adds head-dim elements 4q..4q+3 of query
+                // column m with one 16-byte reduction and a warp instruction covers
+                // four full 128-byte rows.
+                const int m = lane & 3;
+                float* base = a.dq_acc + (((int64_t)x.b * a.H + h) * a.S + (int64_t)i * BT + m) * D +
+                              (warp % 4) * 32 + (lane >> 2) * 4;
                 const int nq = min(BT, a.S - i * BT);
                 // Two halves of 64 query columns (64 registers each); TMEM is
                 // released once the second half has been read.
 #pragma unroll 1
                 for (int hf = 0; hf < 2; ++hf) {
-                    uint32_t v0[32], v1[32];
-                    tmem_ld32x2(tdQ + hf * 64, tdQ + hf * 64 + 32, v0, v1);
+                    uint32_t v[64];
+                    tmem_ld32x2(tdQ + hf * 64, tdQ + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[0]),
+                                *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
                     if (hf == 1) {   // relaxed: the arrival must not wait for the first half's adds
                         tc_fence_before();
                         mbar_arrive_relaxed(dq_free);
                     }
-                    float* bh = base + (int64_t)(hf * 64) * stride;
 #pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        if (hf * 64 + c < nq) atomicAdd(bh + c * stride, __uint_as_float(v0[c]));
-#pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        if (hf * 64 + 32 + c < nq) atomicAdd(bh + (32 + c) * stride, __uint_as_float(v1[c]));
+                    for (int g = 0; g < 16; ++g) {
+                        float xq[4] = {__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
+                                       __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3])};
+                        quad_transpose(xq, lane);
+                        if (hf * 64 + 4 * g + m < nq)
+                            red_add_v4(base + (hf * 64 + 4 * g) * D, xq[0], xq[1], xq[2], xq[3]);
+                    }
                 }
             }
         }

@@ -78,8 +78,23 @@ struct BwdArgs {
     int trace_cap;
 };
 
+// Query tiles of an item are swept upwards for key tiles in the lower half of
+// the sequence and downwards for the upper half.  The balanced list gives a
+// worker a key tile t and then its mirror n-1-t; sweeping both upwards would
+// bring every worker's second item onto the same query tile at the same time
+// (all of them end at the last tile), and their fp32 dQ reductions would then
+// serialise on the same lines.  With the mirror swept downwards, workers stay
+// on distinct tiles of a window of about 150 tiles.  Any order is correct:
+// dK/dV accumulate and the dQ reductions commute.
 struct BItem {
     int b, g, t, i0, n_q, ntiles;
+    bool down;                      // sweep query tiles from the last one down
+    // k-th tile of the item: head hh of the group (0..G-1), query tile i
+    __device__ __forceinline__ void tile(int k, int& hh, int& i) const {
+        const int len = n_q - i0, r = k % len;
+        hh = k / len;
+        i = down ? n_q - 1 - r : i0 + r;
+    }
 };
 
 __device__ __forceinline__ BItem bdecode(const BwdArgs& a, int it) {
@@ -91,6 +106,7 @@ __device__ __forceinline__ BItem bdecode(const BwdArgs& a, int it) {
     x.n_q = (a.S + BT - 1) / BT;
     x.i0 = a.causal ? x.t : 0;
     x.ntiles = (a.H / a.Hkv) * (x.n_q - x.i0);
+    x.down = 2 * x.t >= a.n_units;
     return x;
 }
 
@@ -189,31 +205,31 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 }
             }
             __syncwarp();
-            for (int hh = 0; hh < G && ok; ++hh) {
+            for (int k = 0; k < x.ntiles && ok; ++k, ++n) {
+                int hh, i;
+                x.tile(k, hh, i);
                 const int h = x.g * G + hh;
                 const size_t side_off = ((size_t)x.b * a.H + h) * a.S_pad;
-                for (int i = x.i0; i < x.n_q; ++i, ++n) {
-                    const uint32_t s = n & 1, ph = ((n >> 1) & 1) ^ 1;
-                    if (!wait(&q_empty[s], ph)) break;
-                    ++q_issued;
-                    if (lane == 0) {
-                        mbar_arrive_expect_tx(&q_full[s], C::kTile + kSide);
-                        for (int blk = 0; blk < D / 64; ++blk)
-                            tma_load_4d(sQ + s * C::kTile + blk * 16384, &tmQ, &q_full[s], blk * 64, h, i * BT, x.b);
-                        bulk_load(sSide + s * kSide, a.lse2 + side_off + i * BT, 512, &q_full[s]);
-                        bulk_load(sSide + s * kSide + 512, a.delta + side_off + i * BT, 512, &q_full[s]);
-                    }
-                    __syncwarp();
-                    if (!wait(&do_empty[s], ph)) break;
-                    ++do_issued;
-                    if (lane == 0) {
-                        mbar_arrive_expect_tx(&do_full[s], C::kTile);
-                        for (int blk = 0; blk < D / 64; ++blk)
-                            tma_load_4d(sdO + s * C::kTile + blk * 16384, &tmdO, &do_full[s], blk * 64, h, i * BT,
-                                        x.b);
-                    }
-                    __syncwarp();
+                const uint32_t s = n & 1, ph = ((n >> 1) & 1) ^ 1;
+                if (!wait(&q_empty[s], ph)) break;
+                ++q_issued;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&q_full[s], C::kTile + kSide);
+                    for (int blk = 0; blk < D / 64; ++blk)
+                        tma_load_4d(sQ + s * C::kTile + blk * 16384, &tmQ, &q_full[s], blk * 64, h, i * BT, x.b);
+                    bulk_load(sSide + s * kSide, a.lse2 + side_off + i * BT, 512, &q_full[s]);
+                    bulk_load(sSide + s * kSide + 512, a.delta + side_off + i * BT, 512, &q_full[s]);
                 }
+                __syncwarp();
+                if (!wait(&do_empty[s], ph)) break;
+                ++do_issued;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&do_full[s], C::kTile);
+                    for (int blk = 0; blk < D / 64; ++blk)
+                        tma_load_4d(sdO + s * C::kTile + blk * 16384, &tmdO, &do_full[s], blk * 64, h, i * BT,
+                                    x.b);
+                }
+                __syncwarp();
             }
             ++kvi;
         }
@@ -345,7 +361,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             const int kvg = x.t * BT + r;                   // global key index of this thread's row
             const bool row_ok = kvg < a.S;
             for (int k = 0; k < x.ntiles; ++k, ++n) {
-                const int i = x.i0 + k % (x.n_q - x.i0);
+                int hh, i;
+                x.tile(k, hh, i);
                 const uint32_t s = n & 1, ph = (n >> 1) & 1;
                 if (!wait(&q_full[s], ph, 0) || !wait(s_full, n & 1, 0) || !wait(dp_full, n & 1, 0)) break;
                 tc_fence_after();
@@ -438,7 +455,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         for (int it = it_begin; it < it_end && ok; ++it) {
             const BItem x = bdecode(a, a.wl_items[it]);
             for (int k = 0; k < x.ntiles; ++k, ++n) {
-                const int hh = k / (x.n_q - x.i0), i = x.i0 + k % (x.n_q - x.i0);
+                int hh, i;
+                x.tile(k, hh, i);
                 const int h = x.g * G + hh;
                 ok = __all_sync(0xffffffffu, mbar_wait_acc(dq_full, n & 1, abort_flag, a.err, a.trace ? &wt : nullptr));
                 if (!ok) break;

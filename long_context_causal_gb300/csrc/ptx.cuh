@@ -126,6 +126,55 @@ __device__ __forceinline__ bool mbar_wait_acc(uint64_t* bar, uint32_t parity, vo
     return mbar_wait_slow(bar, parity, abort_flag, err);
 }
 
+// Bulk (TMA) fp32 reduction of a contiguous shared-memory block into global
+// memory: both addresses 16-byte aligned, bytes a multiple of 16.  Tracked by
+// the issuing thread's bulk-group; bulk_wait_read() before the source is
+// rewritten, bulk_wait_all() before the CTA exits.
+__device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, const void* ssrc, uint32_t bytes) {
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst),
+                 "r"(smem_u32(ssrc)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Named barrier over `count` threads (a multiple of 32); id 0 is __syncthreads.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// Named barrier that also ANDs a flag over the participating threads.
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t count, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %3, 0;\n\t"
+        "bar.red.and.pred p, %1, %2, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(id), "r"(count), "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+
+// Vector fp32 reduction into global memory: 16 bytes, 16-byte aligned.
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+// 4 x 4 transpose inside each quad of lanes (lanes 4q..4q+3): on entry lane
+// 4q+j holds x[m] = element (j, m) of its quad's block, on exit lane 4q+m holds
+// x[j] = element (j, m).  Four shuffles.
+__device__ __forceinline__ void quad_transpose(float (&x)[4], int lane) {
+    const bool o1 = lane & 1, o2 = lane & 2;
+    float r0 = __shfl_xor_sync(0xffffffffu, o1 ? x[0] : x[1], 1);
+    float r1 = __shfl_xor_sync(0xffffffffu, o1 ? x[2] : x[3], 1);
+    if (o1) { x[0] = r0; x[2] = r1; } else { x[1] = r0; x[3] = r1; }
+    r0 = __shfl_xor_sync(0xffffffffu, o2 ? x[0] : x[2], 2);
+    r1 = __shfl_xor_sync(0xffffffffu, o2 ? x[1] : x[3], 2);
+    if (o2) { x[0] = r0; x[1] = r1; } else { x[2] = r0; x[3] = r1; }
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
