@@ -61,8 +61,11 @@ def _load():
             lib.oracle_dq_rows.argtypes = [_DP, _DP, _DP, _DP] + dims + [_LP, _I64, _DP, ctypes.c_int]
             lib.oracle_dkv_rows.argtypes = [_DP, _DP, _DP, _DP] + dims + [_LP, _I64, _DP, _DP, ctypes.c_int]
             lib.oracle_merge.argtypes = [_DP, _DP, _DP, _DP, _I64, _I64, _I64, _I64, _DP, _DP]
+            lib.oracle_delta.argtypes = [_DP, _DP, _DP, _DP] + dims + [_DP, ctypes.c_int]
+            lib.oracle_chunk_bwd.argtypes = [_DP, _DP, _DP, _DP, _DP, _DP] + dims + [_DP, _DP, _DP, ctypes.c_int]
             for f in ("oracle_fwd", "oracle_fwd_rows", "oracle_bwd", "oracle_dq_rows",
-                      "oracle_dkv_rows", "oracle_merge", "oracle_num_threads"):
+                      "oracle_dkv_rows", "oracle_merge", "oracle_num_threads", "oracle_delta",
+                      "oracle_chunk_bwd"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -164,6 +167,36 @@ def attn_dkv_rows(q, k, v, dO, krows, *, causal=True, scale=None, q_offset=0, kv
                                  _p(dK), _p(dV), int(threads))
     _check(rc, "dkv_rows")
     return dK, dV
+
+
+def delta(q, k, v, dO, *, causal=True, scale=None, q_offset=0, kv_offset=0, threads=0):
+    """Delta [B,H,Lq] = sum_j P_ij dP_ij over each row's visible keys, fp64."""
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    B, H, Hkv, Lq, Lkv, D = _dims(q, k)
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    out = np.empty((B, H, Lq))
+    rc = _load().oracle_delta(_p(q), _p(k), _p(v), _p(dO), B, H, Hkv, Lq, Lkv, D, q_offset, kv_offset,
+                              int(bool(causal)), scale, _p(out), int(threads))
+    _check(rc, "delta")
+    return out
+
+
+def chunk_bwd(q, k, v, dO, lse, dlt, *, causal=True, scale=None, q_offset=0, kv_offset=0, threads=0):
+    """Backward of one (query chunk, key chunk) pair given the rows' global lse
+    and Delta [B,H,Lq]: partial dQ [B,Lq,H,D] (this chunk's keys), partial dK, dV
+    [B,Lkv,H_kv,D] (this chunk's queries), fp64."""
+    q, k, v, dO, lse, dlt = _f64(q), _f64(k), _f64(v), _f64(dO), _f64(lse), _f64(dlt)
+    B, H, Hkv, Lq, Lkv, D = _dims(q, k)
+    assert lse.shape == (B, H, Lq) and dlt.shape == (B, H, Lq)
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    dQ = np.empty_like(q)
+    dK = np.empty_like(k)
+    dV = np.empty_like(v)
+    rc = _load().oracle_chunk_bwd(_p(q), _p(k), _p(v), _p(dO), _p(lse), _p(dlt), B, H, Hkv, Lq, Lkv, D,
+                                  q_offset, kv_offset, int(bool(causal)), scale, _p(dQ), _p(dK), _p(dV),
+                                  int(threads))
+    _check(rc, "chunk_bwd")
+    return dQ, dK, dV
 
 
 def merge(O_a, lse_a, O_b, lse_b):

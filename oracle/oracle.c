@@ -27,6 +27,10 @@
  *   Delta_i = sum_j P_ij dP_ij            (the explicit definition, not dO.O)
  *   dS_ij = P_ij (dP_ij - Delta_i)
  *   dQ_i  = scale sum_j dS_ij k_j,   dK_j = scale sum_i dS_ij q_i
+ * A worker's backward step for one (query chunk, key chunk) pair (§3.3) uses
+ * the rows' global lse_i and Delta_i and gives the pair's share of dQ (for the
+ * query chunk) and of dK, dV (for the key chunk); summed over the pairs these
+ * are the full gradients (oracle_chunk_bwd).
  * Grouped-query attention (GQA paper, cited on the DISTFLASHATTN page): query
  * head h reads key/value head h / (H / H_kv); dK/dV sum over the group.
  *
@@ -380,4 +384,113 @@ int oracle_merge(const double* Oa, const double* lse_a, const double* Ob, const 
                 lse[(b * H + h) * L + i] = l;
             }
     return 0;
+}
+
+/* Delta_i = sum_j P_ij dP_ij over every visible key of row (b, h, i)
+ * (the explicit definition; equal to <dO_i, O_i>).  delta is [B, H, Lq]. */
+int oracle_delta(const double* q, const double* k, const double* v, const double* dO,
+                 int64_t B, int64_t H, int64_t Hkv, int64_t Lq, int64_t Lkv, int64_t D,
+                 int64_t q_offset, int64_t kv_offset, int causal, double scale,
+                 double* delta, int nthreads) {
+    dims_t d = {B, H, Hkv, Lq, Lkv, D, q_offset, kv_offset, causal, scale};
+    if (check_dims(&d)) return 1;
+    set_threads(nthreads);
+    const int64_t total = B * H * Lq;
+    const int64_t G = H / Hkv;
+    int err = 0;
+#pragma omp parallel
+    {
+        double* p = (double*)malloc(sizeof(double) * (size_t)(Lkv > 0 ? Lkv : 1));
+        if (!p) {
+#pragma omp atomic write
+            err = 2;
+        } else {
+#pragma omp for schedule(dynamic, 16)
+            for (int64_t t = 0; t < total; ++t) {
+                int64_t i = t % Lq, h = (t / Lq) % H, b = t / (Lq * H), g = h / G;
+                double l = score_row(q, k, &d, b, h, i, p);
+                prob_row(&d, p, l, p);
+                const double* doi = qrow(dO, &d, b, i, h);
+                double acc = 0.0;
+                for (int64_t j = 0; j < Lkv; ++j) {
+                    if (p[j] == 0.0) continue;
+                    const double* vj = kvrow(v, &d, b, j, g);
+                    double dp = 0.0;
+                    for (int64_t e = 0; e < D; ++e) dp += doi[e] * vj[e];
+                    acc += p[j] * dp;
+                }
+                delta[(b * H + h) * Lq + i] = acc;
+            }
+        }
+        free(p);
+    }
+    return err;
+}
+
+/* Backward of one (query chunk, key chunk) pair -- the per-worker backward
+ * step of DISTFLASHATTN §3.3 (the helper's partial gradients, computed from
+ * the owner's saved output statistics).  The rows' lse_i and Delta_i are the
+ * global ones (over the whole key sequence), given as inputs [B, H, Lq].  For
+ * the pair's visible (i, j):
+ *   P_ij = exp(s_ij - lse_i),  dS_ij = P_ij (<dO_i, v_j> - Delta_i)
+ *   dQ_i = scale sum_j dS_ij k_j,  dK_j = scale sum_i dS_ij q_i,  dV_j = sum_i P_ij dO_i
+ * restricted to this chunk's keys (dQ) and queries (dK, dV).  Summed over the
+ * key chunks (dQ) or query chunks (dK, dV) they are the full gradients.
+ * Outputs are overwritten.  A row with lse_i = -inf contributes nothing. */
+int oracle_chunk_bwd(const double* q, const double* k, const double* v, const double* dO,
+                     const double* lse, const double* delta,
+                     int64_t B, int64_t H, int64_t Hkv, int64_t Lq, int64_t Lkv, int64_t D,
+                     int64_t q_offset, int64_t kv_offset, int causal, double scale,
+                     double* dQ, double* dK, double* dV, int nthreads) {
+    dims_t d = {B, H, Hkv, Lq, Lkv, D, q_offset, kv_offset, causal, scale};
+    if (check_dims(&d)) return 1;
+    set_threads(nthreads);
+    const int64_t kvn = B * Lkv * Hkv * D;
+    memset(dK, 0, sizeof(double) * (size_t)kvn);
+    memset(dV, 0, sizeof(double) * (size_t)kvn);
+    const int64_t total = B * H * Lq;
+    const int64_t G = H / Hkv;
+    int err = 0;
+#pragma omp parallel
+    {
+        double* lk = (double*)calloc((size_t)(kvn > 0 ? kvn : 1), sizeof(double));
+        double* lv = (double*)calloc((size_t)(kvn > 0 ? kvn : 1), sizeof(double));
+        if (!lk || !lv) {
+#pragma omp atomic write
+            err = 2;
+        } else {
+#pragma omp for schedule(dynamic, 16)
+            for (int64_t t = 0; t < total; ++t) {
+                int64_t i = t % Lq, h = (t / Lq) % H, b = t / (Lq * H), g = h / G;
+                const double* qi = qrow(q, &d, b, i, h);
+                const double* doi = qrow(dO, &d, b, i, h);
+                const double li = lse[(b * H + h) * Lq + i], di = delta[(b * H + h) * Lq + i];
+                double* dqi = dQ + ((b * Lq + i) * H + h) * D;
+                for (int64_t e = 0; e < D; ++e) dqi[e] = 0.0;
+                if (li == -INFINITY) continue;
+                for (int64_t j = 0; j < Lkv; ++j) {
+                    if (!visible(&d, i, j)) continue;
+                    const double* kj = kvrow(k, &d, b, j, g);
+                    const double* vj = kvrow(v, &d, b, j, g);
+                    double s = 0.0, dp = 0.0;
+                    for (int64_t e = 0; e < D; ++e) { s += qi[e] * kj[e]; dp += doi[e] * vj[e]; }
+                    const double p = exp(scale * s - li);
+                    const double ds = p * (dp - di);
+                    double* lkj = lk + ((b * Lkv + j) * Hkv + g) * D;
+                    double* lvj = lv + ((b * Lkv + j) * Hkv + g) * D;
+                    for (int64_t e = 0; e < D; ++e) {
+                        dqi[e] += scale * ds * kj[e];
+                        lkj[e] += scale * ds * qi[e];
+                        lvj[e] += p * doi[e];
+                    }
+                }
+            }
+#pragma omp critical
+            {
+                for (int64_t x = 0; x < kvn; ++x) { dK[x] += lk[x]; dV[x] += lv[x]; }
+            }
+        }
+        free(lk); free(lv);
+    }
+    return err;
 }

@@ -154,6 +154,59 @@ def test_merging_chunk_partials_equals_monolithic(P):
         np.testing.assert_allclose(acc[1], lse_ref[:, :, p * C:(p + 1) * C], atol=1e-13)
 
 
+# ---------------------------------------------------------------- chunk-pair backward (§3.3)
+def chunk_bounds(S, cuts):
+    edges = [0] + list(cuts) + [S]
+    return list(zip(edges[:-1], edges[1:]))
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("cuts", [(), (12,), (5, 13), (4, 8, 16)])
+def test_chunk_pair_backward_sums_to_full(cuts, causal):
+    # Each worker's backward step gives partial dQ for its query chunk and partial
+    # dK/dV for the key chunk it visits, from the rows' global lse and Delta; the
+    # sum over the pairs must be the full gradient (pinned by finite differences).
+    B, H, Hkv, S, D = 2, 4, 2, 21, 5
+    q, k, v = rnd((B, S, H, D), 300), rnd((B, S, Hkv, D), 301), rnd((B, S, Hkv, D), 302)
+    dO = rnd((B, S, H, D), 303)
+    kw = dict(causal=causal, scale=0.6)
+    _, lse = oracle.attn_fwd(q, k, v, **kw)
+    dlt = oracle.delta(q, k, v, dO, **kw)
+    dQ_ref, dK_ref, dV_ref = oracle.attn_bwd(q, k, v, dO, **kw)
+    dQ, dK, dV = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    chunks = chunk_bounds(S, cuts)
+    for qa, qb in chunks:
+        for ka, kb in chunks:
+            pq, pk, pv = oracle.chunk_bwd(q[:, qa:qb], k[:, ka:kb], v[:, ka:kb], dO[:, qa:qb],
+                                          lse[:, :, qa:qb], dlt[:, :, qa:qb],
+                                          q_offset=qa, kv_offset=ka, **kw)
+            dQ[:, qa:qb] += pq
+            dK[:, ka:kb] += pk
+            dV[:, ka:kb] += pv
+    np.testing.assert_allclose(dQ, dQ_ref, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(dK, dK_ref, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(dV, dV_ref, atol=1e-12, rtol=0)
+
+
+def test_delta_equals_dO_dot_O():
+    # sum_j P_ij <dO_i, v_j> = <dO_i, sum_j P_ij v_j> = <dO_i, O_i>
+    B, H, Hkv, S, D = 1, 3, 1, 9, 4
+    q, k, v, dO = rnd((B, S, H, D), 310), rnd((B, S, Hkv, D), 311), rnd((B, S, Hkv, D), 312), rnd((B, S, H, D), 313)
+    O, _ = oracle.attn_fwd(q, k, v)
+    np.testing.assert_allclose(oracle.delta(q, k, v, dO), np.einsum("bshd,bshd->bhs", O, dO), atol=1e-13)
+
+
+def test_chunk_pair_above_the_diagonal_contributes_nothing():
+    q, k, v, dO = rnd((1, 4, 2, 3), 320), rnd((1, 4, 1, 3), 321), rnd((1, 4, 1, 3), 322), rnd((1, 4, 2, 3), 323)
+    lse, dlt = rnd((1, 2, 4), 324), rnd((1, 2, 4), 325)
+    for out in oracle.chunk_bwd(q, k, v, dO, lse, dlt, q_offset=0, kv_offset=4):
+        assert np.all(out == 0.0)
+    # and a row whose global lse is -inf (no visible key anywhere) adds nothing
+    lse[0, 1, 2] = -np.inf
+    pq, _, _ = oracle.chunk_bwd(q, k, v, dO, lse, dlt, q_offset=4, kv_offset=0)
+    assert np.all(pq[0, 2, 1] == 0.0)
+
+
 def test_merge_neutral_element_and_symmetry():
     O_a, O_b = rnd((1, 3, 2, 4), 80), rnd((1, 3, 2, 4), 81)
     la, lb = rnd((1, 2, 3), 82), rnd((1, 2, 3), 83)
