@@ -91,6 +91,38 @@ dfa_status dfa_merge_partials(int B, int H, int L, int D,
                               const float* O_b, const float* lse_b,
                               float* O_out, float* lse_out, void* stream);
 
+/* Backward step for one (query chunk, key chunk) pair -- the per-worker
+ * backward of DISTFLASHATTN §3.3: the owner's saved output O and log-sum-exp
+ * of its query rows (global, over the whole key sequence, as returned by the
+ * forward and its merges) are reused, never recomputed.  With
+ *   P_ij = exp(scale <q_i, k_j> - lse_i),  Delta_i = <dO_i, O_i>,
+ *   dS_ij = P_ij (<dO_i, v_j> - Delta_i)   for the pair's visible (i, j)
+ * it ADDS this pair's share to three fp32 accumulators:
+ *   dQ_acc[i] += scale sum_j dS_ij k_j,  dK_acc[j] += scale sum_i dS_ij q_i,
+ *   dV_acc[j] += sum_i P_ij dO_i
+ * so that summing the pairs over all key chunks (dQ) and all query chunks
+ * (dK, dV) gives the full gradients.
+ *   q, O, dO: [B, Lq, H, D] dense in dt;  k, v: [B, Lkv, H_kv, D] dense in dt
+ *   lse:      fp32 [B, H, Lq], natural log (the rows' final lse)
+ *   causal:   1 = pairs with kv_offset + j > q_offset + i are skipped
+ *   dQ_acc:   fp32 [B, Lq, H, D];  dK_acc, dV_acc: fp32 [B, Lkv, H_kv, D];
+ *             all caller-owned, updated in place (+=), never cleared
+ *   workspace: >= dfa_chunk_bwd_workspace_size(...) bytes, 256-byte aligned,
+ *             caller-owned scratch (contents not preserved)
+ * bf16 with D = 128 and kv_offset - q_offset a multiple of 128 runs on the
+ * tensor cores; other cases on the CUDA-core kernels.  Errors: INVALID_ARG
+ * for bad sizes, offsets, pointers or workspace; nothing is launched then.
+ * Calls on one stream may share accumulators; concurrent calls must not. */
+dfa_status dfa_chunk_attn_bwd(const void* q, const void* k, const void* v, const void* O,
+                              const float* lse, const void* dO, dfa_dtype dt,
+                              int B, int H, int H_kv, int Lq, int Lkv, int D,
+                              int64_t q_offset, int64_t kv_offset, int causal, float scale,
+                              float* dQ_acc, float* dK_acc, float* dV_acc,
+                              void* workspace, size_t ws_bytes, void* stream);
+
+/* Bytes of workspace dfa_chunk_attn_bwd needs (0 for invalid sizes). */
+size_t dfa_chunk_bwd_workspace_size(int B, int H, int H_kv, int Lq, int Lkv, int D);
+
 /* Bytes of workspace dfa_attn_fwd (bwd = 0) or dfa_attn_bwd (bwd = 1) needs.
  * Returns 0 for invalid sizes. */
 size_t dfa_attn_workspace_size(int B, int H, int H_kv, int S, int D, int n_chunks, int bwd);

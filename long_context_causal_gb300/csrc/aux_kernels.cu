@@ -161,14 +161,21 @@ __global__ void convert_bf16_kernel(int64_t n, int H, int S, int D, float scale,
 }
 
 __global__ void convert_f32_kernel(int64_t n, int H, int S, int D, float scale, const float* __restrict__ in,
-                                   float* __restrict__ out) {
+                                   float* __restrict__ out, int accumulate) {
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < n / 8; x += stride) {
         const float4* src = reinterpret_cast<const float4*>(in + acc_index(8 * x, H, S, D));
         const float4 a = src[0], b = src[1];
         float4* dst = reinterpret_cast<float4*>(out) + 2 * x;
-        dst[0] = make_float4(scale * a.x, scale * a.y, scale * a.z, scale * a.w);
-        dst[1] = make_float4(scale * b.x, scale * b.y, scale * b.z, scale * b.w);
+        float4 o0 = make_float4(scale * a.x, scale * a.y, scale * a.z, scale * a.w);
+        float4 o1 = make_float4(scale * b.x, scale * b.y, scale * b.z, scale * b.w);
+        if (accumulate) {
+            const float4 p0 = dst[0], p1 = dst[1];
+            o0.x += p0.x; o0.y += p0.y; o0.z += p0.z; o0.w += p0.w;
+            o1.x += p1.x; o1.y += p1.y; o1.z += p1.z; o1.w += p1.w;
+        }
+        dst[0] = o0;
+        dst[1] = o1;
     }
 }
 
@@ -217,14 +224,14 @@ dfa_status launch_bwd_prep(dfa_dtype dt, int B, int H, int S, int S_pad, int D, 
 }
 
 dfa_status launch_convert(dfa_dtype dt, int B, int H, int S, int D, float scale, const float* acc, void* out,
-                          cudaStream_t s) {
+                          bool accumulate, cudaStream_t s) {
     const int64_t n = (int64_t)B * S * H * D;
     if (n == 0) return DFA_OK;
     const int blocks = 8 * num_sms();
-    if (dt == DFA_BF16)
+    if (dt == DFA_BF16 && !accumulate)
         convert_bf16_kernel<<<blocks, kThreads, 0, s>>>(n, H, S, D, scale, acc, (__nv_bfloat16*)out);
     else
-        convert_f32_kernel<<<blocks, kThreads, 0, s>>>(n, H, S, D, scale, acc, (float*)out);
+        convert_f32_kernel<<<blocks, kThreads, 0, s>>>(n, H, S, D, scale, acc, (float*)out, accumulate);
     return launched("convert");
 }
 

@@ -59,13 +59,15 @@ static_assert(kSmem <= 232448, "shared memory");
 constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384;
 
 struct Args {
-    int B, H, Hkv, S, S_pad, causal;
+    int B, H, Hkv, Lq, Lkv, S_pad, causal;
+    int rel;                      // kv_offset - q_offset (a multiple of 128)
+    int acc_f32;                  // dK/dV: fp32 accumulate (+=) instead of bf16 store
     float scale, c2;
     const float* lse2;
     const float* delta;
     float* dq_acc;                // [B, H, S, D] fp32, zeroed by the caller
-    __nv_bfloat16* dK;
-    __nv_bfloat16* dV;
+    void* dK;                     // [B, Lkv, Hkv, D]
+    void* dV;
     const int32_t* wl_offsets;
     const int32_t* wl_items;
     int n_units;
@@ -99,8 +101,9 @@ __device__ __forceinline__ Item decode(const Args& a, int it) {
     x.b = row / a.Hkv;
     x.g = row % a.Hkv;
     x.t = a.n_units - 1 - unit;
-    x.n_q = (a.S + BT - 1) / BT;
-    x.i0 = a.causal ? x.t : 0;
+    x.n_q = (a.Lq + BT - 1) / BT;
+    // first query tile that sees any key of tile t: q_offset + 128 i + 127 >= kv_offset + 128 t
+    x.i0 = a.causal ? min(max(x.t + a.rel / BT, 0), x.n_q) : 0;
     x.ntiles = (a.H / a.Hkv) * (x.n_q - x.i0);
     x.down = 2 * x.t >= a.n_units;
     return x;
@@ -189,6 +192,7 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         };
         for (int it = it_begin; it < it_end && ok; ++it) {
             const Item x = decode(a, a.wl_items[it]);
+            if (x.ntiles == 0) continue;   // key tile entirely above the diagonal: nothing to do
             if (!wait(kv_empty, (kvi & 1) ^ 1)) break;
             ++kv_issued;
             if (lane == 0) {
@@ -286,6 +290,7 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         };
         for (int it = it_begin; it < it_end && ok; ++it) {
             const Item x = decode(a, a.wl_items[it]);
+            if (x.ntiles == 0) continue;   // key tile entirely above the diagonal: nothing to do
             if (!wait(kv_full, kvi & 1, 0)) break;
             if (!issue_S(n) || !issue_dP(n)) break;
             for (int k = 0; k < x.ntiles && ok; ++k, ++n) {
@@ -352,8 +357,9 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         };
         for (int it = it_begin; it < it_end && ok; ++it) {
             const Item x = decode(a, a.wl_items[it]);
+            if (x.ntiles == 0) continue;   // key tile entirely above the diagonal: nothing to do
             const int kvg = x.t * BT + r;
-            const bool row_ok = kvg < a.S;
+            const bool row_ok = kvg < a.Lkv;
             for (int k = 0; k < x.ntiles; ++k, ++n) {
                 int h, i;
                 x.tile(k, G, h, i);
@@ -366,7 +372,8 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 const float* dl = lse2 + BT;
                 // Elements outside the causal triangle or the sequence only occur on
                 // the diagonal tile and on ragged edges; elsewhere no mask is applied.
-                const bool full = !(a.causal && i == x.t) && (i + 1) * BT <= a.S && (x.t + 1) * BT <= a.S;
+                const bool full = !(a.causal && i == x.t + a.rel / BT) && (i + 1) * BT <= a.Lq &&
+                                  (x.t + 1) * BT <= a.Lkv;
                 // ---- phase 1: P^T = exp2(S^T c - lse2) -> TMEM (bf16) and registers
                 uint32_t u[32], pk[32];
 #pragma unroll
@@ -376,7 +383,7 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
                         for (int z = 0; z < 32; ++z) {
                             const int qg = q0 + c + z;
-                            if (!(row_ok && qg < a.S && !(a.causal && kvg > qg))) u[z] = 0xff800000u;
+                            if (!(row_ok && qg < a.Lq && !(a.causal && kvg + a.rel > qg))) u[z] = 0xff800000u;
                         }
                     }
 #pragma unroll
@@ -421,17 +428,35 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 mbar_arrive(ds_done);
             }
             if (!ok) break;
-            // ---- epilogue: dV = acc, dK = scale * acc, bf16 [B, S, Hkv, D]; this half's columns
+            // ---- epilogue: dV = acc, dK = scale * acc into [B, Lkv, Hkv, D] (bf16 store,
+            // or fp32 += for a chunk pair's partial gradients); this half's columns
             if (!wait(kd_full, kvi & 1, 1)) break;
             tc_fence_after();
-            const int64_t orow = (((int64_t)x.b * a.S + kvg) * a.Hkv + x.g) * D;
+            const int64_t orow = (((int64_t)x.b * a.Lkv + kvg) * a.Hkv + x.g) * D;
 #pragma unroll 1
             for (int c = half * 2; c < half * 2 + 2; ++c) {
                 uint32_t uv[32], uk[32];
                 tmem_ld32x2(tmem + lane_base + kColDV + c * 32, tmem + lane_base + kColDK + c * 32, uv, uk);
-                if (row_ok) {
-                    uint4* pv = reinterpret_cast<uint4*>(a.dV + orow + c * 32);
-                    uint4* pkk = reinterpret_cast<uint4*>(a.dK + orow + c * 32);
+                if (row_ok && a.acc_f32) {
+                    float4* pv = reinterpret_cast<float4*>(static_cast<float*>(a.dV) + orow + c * 32);
+                    float4* pkk = reinterpret_cast<float4*>(static_cast<float*>(a.dK) + orow + c * 32);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        float4 v = pv[e], w = pkk[e];
+                        v.x += __uint_as_float(uv[4 * e]);
+                        v.y += __uint_as_float(uv[4 * e + 1]);
+                        v.z += __uint_as_float(uv[4 * e + 2]);
+                        v.w += __uint_as_float(uv[4 * e + 3]);
+                        w.x += a.scale * __uint_as_float(uk[4 * e]);
+                        w.y += a.scale * __uint_as_float(uk[4 * e + 1]);
+                        w.z += a.scale * __uint_as_float(uk[4 * e + 2]);
+                        w.w += a.scale * __uint_as_float(uk[4 * e + 3]);
+                        pv[e] = v;
+                        pkk[e] = w;
+                    }
+                } else if (row_ok) {
+                    uint4* pv = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dV) + orow + c * 32);
+                    uint4* pkk = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dK) + orow + c * 32);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         uint4 v, w;
@@ -467,6 +492,7 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         uint64_t wt = 0;
         for (int it = it_begin; it < it_end && ok; ++it) {
             const Item x = decode(a, a.wl_items[it]);
+            if (x.ntiles == 0) continue;   // key tile entirely above the diagonal: nothing to do
             for (int k = 0; k < x.ntiles; ++k, ++n) {
                 int h, i;
                 x.tile(k, G, h, i);
@@ -479,9 +505,9 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 // column m with one 16-byte reduction and a warp instruction covers
                 // four full 128-byte rows.
                 const int m = lane & 3;
-                float* base = a.dq_acc + (((int64_t)x.b * a.H + h) * a.S + (int64_t)i * BT + m) * D +
+                float* base = a.dq_acc + (((int64_t)x.b * a.H + h) * a.Lq + (int64_t)i * BT + m) * D +
                               (warp % 4) * 32 + (lane >> 2) * 4;
-                const int nq = min(BT, a.S - i * BT);
+                const int nq = min(BT, a.Lq - i * BT);
                 // Two halves of 64 query columns (64 registers each); TMEM is
                 // released once the second half has been read.
 #pragma unroll 1
@@ -520,8 +546,11 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
 dfa_status tc_bwd_pipelined(const AttnProblem& p, const void* q, const void* k, const void* v, const void* dO,
                             const float* lse2, const float* delta, int S_pad, float* dq_acc, void* dK, void* dV,
-                            const WorkList* wl, cudaStream_t s) {
+                            bool acc_f32, const WorkList* wl, cudaStream_t s) {
     if (p.D != D) return fail(DFA_ERR_UNSUPPORTED, "pipelined backward needs D = 128");
+    const int64_t rel = p.kv_offset - p.q_offset;
+    if (rel % BT != 0 || rel > (int64_t)1 << 30 || rel < -((int64_t)1 << 30))
+        return fail(DFA_ERR_UNSUPPORTED, "tensor-core backward needs kv_offset - q_offset a multiple of 128");
     alignas(64) CUtensorMap mq, mk, mv, mdo;
     if (!make_tmap_bshd(&mq, q, p.B, p.Lq, p.H, D, p.q_sb, p.q_ss, p.q_sh) ||
         !make_tmap_bshd(&mdo, dO, p.B, p.Lq, p.H, D, p.q_sb, p.q_ss, p.q_sh) ||
@@ -529,11 +558,12 @@ dfa_status tc_bwd_pipelined(const AttnProblem& p, const void* q, const void* k, 
         !make_tmap_bshd(&mv, v, p.B, p.Lkv, p.Hkv, D, p.kv_sb, p.kv_ss, p.kv_sh))
         return fail(DFA_ERR_CUDA, "tensor map encoding failed");
     Args a{};
-    a.B = p.B; a.H = p.H; a.Hkv = p.Hkv; a.S = p.Lq; a.S_pad = S_pad; a.causal = p.causal;
+    a.B = p.B; a.H = p.H; a.Hkv = p.Hkv; a.Lq = p.Lq; a.Lkv = p.Lkv; a.S_pad = S_pad; a.causal = p.causal;
+    a.rel = (int)rel; a.acc_f32 = acc_f32;
     a.scale = p.scale; a.c2 = p.scale * 1.4426950408889634f;
     a.lse2 = lse2; a.delta = delta; a.dq_acc = dq_acc;
-    a.dK = static_cast<__nv_bfloat16*>(dK);
-    a.dV = static_cast<__nv_bfloat16*>(dV);
+    a.dK = dK;
+    a.dV = dV;
     a.wl_offsets = wl->offsets; a.wl_items = wl->items; a.n_units = wl->n_units;
     a.err = device_error_flag();
     a.trace = cta_trace(&a.trace_cap);

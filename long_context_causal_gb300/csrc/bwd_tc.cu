@@ -537,7 +537,7 @@ dfa_status tc_bwd(const AttnProblem& p, const void* q, const void* k, const void
                   const WorkList* wl, cudaStream_t s) {
     if (p.B == 0 || p.Lq == 0) return DFA_OK;
     // Head dim 128 takes the two-stream pipelined kernel (bwd_pipe_tc.cu).
-    if (p.D == 128) return tc_bwd_pipelined(p, q, k, v, dO, lse2, delta, S_pad, dq_acc, dK, dV, wl, s);
+    if (p.D == 128) return tc_bwd_pipelined(p, q, k, v, dO, lse2, delta, S_pad, dq_acc, dK, dV, false, wl, s);
     return launch<64>(p, q, k, v, dO, lse2, delta, S_pad, dq_acc, dK, dV, wl, s);
 }
 

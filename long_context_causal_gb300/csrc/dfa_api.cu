@@ -334,7 +334,88 @@ extern "C" dfa_status dfa_attn_bwd(const void* q, const void* k, const void* v, 
     WorkList wl{dev, dev + workers + 1, workers, units};
     if ((st = tc_bwd(p, q, k, v, dO, lse2, delta, L.S_pad, dq_acc, dK, dV, &wl, s))) return st;
     count_launch(DFA_KERNEL_BWD);
-    st = launch_convert(dt, B, H, S, D, scale, dq_acc, dQ, s);
+    st = launch_convert(dt, B, H, S, D, scale, dq_acc, dQ, false, s);
+    if (st == DFA_OK) count_launch(DFA_KERNEL_CONVERT);
+    return st;
+}
+
+// ---------------------------------------------------------------- chunk-pair backward
+struct ChunkLayout {
+    size_t delta = 0, lse2 = 0, dq = 0, wl = 0, total = 0;
+    int Lq_pad = 0;
+};
+
+ChunkLayout chunk_layout(int B, int H, int Hkv, int Lq, int Lkv, int D) {
+    ChunkLayout L;
+    size_t off = 0;
+    L.Lq_pad = (Lq + kBwdUnitRows - 1) / kBwdUnitRows * kBwdUnitRows;
+    L.delta = off;
+    off = align_up(off + sizeof(float) * (size_t)B * H * L.Lq_pad);
+    L.lse2 = off;
+    off = align_up(off + sizeof(float) * (size_t)B * H * L.Lq_pad);
+    L.dq = off;
+    off = align_up(off + sizeof(float) * (size_t)B * Lq * H * D);
+    L.wl = off;
+    const size_t units = (size_t)(Lkv + kBwdUnitRows - 1) / kBwdUnitRows;
+    off = align_up(off + sizeof(int32_t) * (kMaxWorkers + 1 + (size_t)B * Hkv * units));
+    L.total = off;
+    return L;
+}
+
+extern "C" size_t dfa_chunk_bwd_workspace_size(int B, int H, int H_kv, int Lq, int Lkv, int D) {
+    if (B < 0 || H <= 0 || H_kv <= 0 || Lq < 0 || Lkv < 0 || (D != 64 && D != 128) || H % H_kv != 0) return 0;
+    return chunk_layout(B, H, H_kv, Lq, Lkv, D).total;
+}
+
+extern "C" dfa_status dfa_chunk_attn_bwd(const void* q, const void* k, const void* v, const void* O,
+                                         const float* lse, const void* dO, dfa_dtype dt, int B, int H, int H_kv,
+                                         int Lq, int Lkv, int D, int64_t q_offset, int64_t kv_offset, int causal,
+                                         float scale, float* dQ_acc, float* dK_acc, float* dV_acc,
+                                         void* workspace, size_t ws_bytes, void* stream) {
+    g_msg[0] = 0;
+    dfa_status st;
+    if ((st = check_dtype(dt)) || (st = check_common(B, H, H_kv, D, scale))) return st;
+    if (Lq < 0 || Lkv < 0) return fail(DFA_ERR_INVALID_ARG, "negative chunk length");
+    if (q_offset < 0 || kv_offset < 0) return fail(DFA_ERR_INVALID_ARG, "negative chunk offset");
+    if ((int64_t)B * Lq == 0 || Lkv == 0) return DFA_OK;   // nothing to add
+    if ((st = check_ptrs({q, k, v, O, lse, dO, dQ_acc, dK_acc, dV_acc}))) return st;
+    const ChunkLayout L = chunk_layout(B, H, H_kv, Lq, Lkv, D);
+    if (!workspace || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return fail(DFA_ERR_INVALID_ARG, "workspace needs %zu bytes, 256-byte aligned (got %zu)", L.total, ws_bytes);
+    AttnProblem p{};
+    p.B = B; p.H = H; p.Hkv = H_kv; p.Lq = Lq; p.Lkv = Lkv; p.D = D;
+    p.q_sb = (int64_t)Lq * H * D; p.q_ss = (int64_t)H * D; p.q_sh = D;
+    p.kv_sb = (int64_t)Lkv * H_kv * D; p.kv_ss = (int64_t)H_kv * D; p.kv_sh = D;
+    p.q_offset = q_offset; p.kv_offset = kv_offset; p.causal = causal != 0; p.scale = scale;
+    p.acc_out = 1;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* ws = static_cast<char*>(workspace);
+    float* delta = reinterpret_cast<float*>(ws + L.delta);
+    const bool tc = dt == DFA_BF16 && D == 128 && (kv_offset - q_offset) % kBwdUnitRows == 0;
+    if (!tc) {
+        if ((st = launch_delta(dt, B, H, Lq, D, O, dO, delta, s))) return st;
+        count_launch(DFA_KERNEL_DELTA);
+        st = simt_bwd(p, dt, q, k, v, dO, lse, delta, dQ_acc, dK_acc, dV_acc, s);
+        if (st == DFA_OK) count_launch(DFA_KERNEL_BWD, 2);
+        return st;
+    }
+    float* lse2 = reinterpret_cast<float*>(ws + L.lse2);
+    if ((st = launch_bwd_prep(dt, B, H, Lq, L.Lq_pad, D, O, dO, lse, lse2, delta, s))) return st;
+    count_launch(DFA_KERNEL_DELTA);
+    float* dq = reinterpret_cast<float*>(ws + L.dq);
+    cudaError_t e = cudaMemsetAsync(dq, 0, sizeof(float) * (size_t)B * Lq * H * D, s);
+    if (e != cudaSuccess) return fail(DFA_ERR_CUDA, "dQ accumulator clear: %s", cudaGetErrorString(e));
+    const int units = (Lkv + kBwdUnitRows - 1) / kBwdUnitRows;
+    const int workers = std::min(num_sms(), B * H_kv * units);
+    const CachedList* c = get_list(B * H_kv, units, workers, DFA_SCHED_BALANCED);
+    if (!c) return fail(DFA_ERR_CUDA, "could not build the work list");
+    int32_t* dev = reinterpret_cast<int32_t*>(ws + L.wl);
+    if ((st = upload_list(c, dev, s))) return st;
+    WorkList wl{dev, dev + workers + 1, workers, units};
+    if ((st = tc_bwd_pipelined(p, q, k, v, dO, lse2, delta, L.Lq_pad, dq, dK_acc, dV_acc, true, &wl, s)))
+        return st;
+    count_launch(DFA_KERNEL_BWD);
+    st = launch_convert(DFA_F32, B, H, Lq, D, scale, dq, dQ_acc, true, s);
     if (st == DFA_OK) count_launch(DFA_KERNEL_CONVERT);
     return st;
 }

@@ -18,6 +18,7 @@ struct AttnProblem {
     int64_t q_offset, kv_offset;  // global token positions of row 0
     int causal;
     float scale;
+    int acc_out;                  // backward outputs are fp32 accumulators (+=)
 };
 
 // Device error flag (set by bounded waits that gave up).  Returns the device
@@ -32,6 +33,7 @@ dfa_status fail(dfa_status st, const char* fmt, ...);
 dfa_status simt_fwd(const AttnProblem& p, dfa_dtype dt, const void* q, const void* k,
                     const void* v, void* O, bool O_is_f32, float* lse, cudaStream_t s);
 // Backward pieces: dQ (dense, dtype dt), dK/dV (dense, dtype dt).  Needs Delta.
+// With p.acc_out set, dQ/dK/dV are fp32 and the results are added to them.
 dfa_status simt_bwd(const AttnProblem& p, dfa_dtype dt, const void* q, const void* k,
                     const void* v, const void* dO, const float* lse, const float* delta,
                     void* dQ, void* dK, void* dV, cudaStream_t s);
@@ -48,8 +50,9 @@ dfa_status launch_bwd_prep(dfa_dtype dt, int B, int H, int S, int S_pad, int D, 
                            const void* dO, const float* lse, float* lse2, float* delta, cudaStream_t s);
 // out[b, s, h, :] = scale * acc[b, h, s, :] cast to dt (acc is the head-major
 // fp32 dQ accumulator of the tensor-core backward; D a multiple of 8).
+// With accumulate, out is fp32 and the scaled values are added to it.
 dfa_status launch_convert(dfa_dtype dt, int B, int H, int S, int D, float scale, const float* acc, void* out,
-                          cudaStream_t s);
+                          bool accumulate, cudaStream_t s);
 
 // ---- tcgen05 tensor-core kernels (fwd_tc.cu, bwd_tc.cu) ----
 struct WorkList {
@@ -68,9 +71,12 @@ dfa_status tc_bwd(const AttnProblem& p, const void* q, const void* k, const void
 
 // Head-dim-128 backward with the softmax-gradient split into two phases so the
 // tensor cores overlap it (bwd_pipe_tc.cu).
+// Problems with Lq != Lkv and offsets (kv_offset - q_offset a multiple of 128)
+// are the chunk-pair backward; acc_f32 makes dK/dV fp32 accumulators (+=).
 dfa_status tc_bwd_pipelined(const AttnProblem& p, const void* q, const void* k, const void* v,
                             const void* dO, const float* lse2, const float* delta, int S_pad,
-                            float* dq_acc, void* dK, void* dV, const WorkList* wl, cudaStream_t s);
+                            float* dq_acc, void* dK, void* dV, bool acc_f32, const WorkList* wl,
+                            cudaStream_t s);
 
 int num_sms();
 

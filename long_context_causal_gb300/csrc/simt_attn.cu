@@ -37,6 +37,8 @@ template <> __device__ __forceinline__ void st<float>(float* p, float x) { *p = 
 template <> __device__ __forceinline__ void st<__nv_bfloat16>(__nv_bfloat16* p, float x) {
     *p = __float2bfloat16_rn(x);
 }
+// Store, or add to the value already there (each output element has one writer).
+template <typename T> __device__ __forceinline__ void put(T* p, float x, bool acc) { st(p, acc ? ld(p) + x : x); }
 
 __device__ __forceinline__ int64_t mn64(int64_t a, int64_t b) { return a < b ? a : b; }
 __device__ __forceinline__ int64_t mx64(int64_t a, int64_t b) { return a > b ? a : b; }
@@ -146,11 +148,11 @@ simt_fwd_kernel(AttnProblem p, const T* __restrict__ q, const T* __restrict__ k,
 }
 
 // ---------------------------------------------------------------- backward: dQ
-template <typename T, int D>
+template <typename T, typename OT, int D>
 __global__ void __launch_bounds__(NWARP * 32)
 simt_bwd_dq_kernel(AttnProblem p, const T* __restrict__ q, const T* __restrict__ k,
                    const T* __restrict__ v, const T* __restrict__ dO, const float* __restrict__ lse,
-                   const float* __restrict__ delta, T* __restrict__ dQ) {
+                   const float* __restrict__ delta, OT* __restrict__ dQ) {
     extern __shared__ float smem[];
     float(*Qs)[D + 1] = reinterpret_cast<float(*)[D + 1]>(smem);
     float(*dOs)[D + 1] = Qs + BQ;
@@ -221,18 +223,18 @@ simt_bwd_dq_kernel(AttnProblem p, const T* __restrict__ q, const T* __restrict__
     for (int r = 0; r < RPW; ++r) {
         const int i = q0 + warp * RPW + r;
         if (i >= p.Lq) continue;
-        T* row = dQ + (((int64_t)b * p.Lq + i) * p.H + h) * D;
+        OT* row = dQ + (((int64_t)b * p.Lq + i) * p.H + h) * D;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) st(row + lane + 32 * c, p.scale * acc[r][c]);
+        for (int c = 0; c < D / 32; ++c) put(row + lane + 32 * c, p.scale * acc[r][c], p.acc_out);
     }
 }
 
 // ---------------------------------------------------------------- backward: dK, dV
-template <typename T, int D>
+template <typename T, typename OT, int D>
 __global__ void __launch_bounds__(NWARP * 32)
 simt_bwd_dkv_kernel(AttnProblem p, const T* __restrict__ q, const T* __restrict__ k,
                     const T* __restrict__ v, const T* __restrict__ dO, const float* __restrict__ lse,
-                    const float* __restrict__ delta, T* __restrict__ dK, T* __restrict__ dV) {
+                    const float* __restrict__ delta, OT* __restrict__ dK, OT* __restrict__ dV) {
     extern __shared__ float smem[];
     float(*Ks)[D + 1] = reinterpret_cast<float(*)[D + 1]>(smem);
     float(*Vs)[D + 1] = Ks + BK;
@@ -311,12 +313,12 @@ simt_bwd_dkv_kernel(AttnProblem p, const T* __restrict__ q, const T* __restrict_
     for (int r = 0; r < RPW; ++r) {
         const int j = j0 + warp * RPW + r;
         if (j >= p.Lkv) continue;
-        T* krow = dK + (((int64_t)b * p.Lkv + j) * p.Hkv + g) * D;
-        T* vrow = dV + (((int64_t)b * p.Lkv + j) * p.Hkv + g) * D;
+        OT* krow = dK + (((int64_t)b * p.Lkv + j) * p.Hkv + g) * D;
+        OT* vrow = dV + (((int64_t)b * p.Lkv + j) * p.Hkv + g) * D;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
-            st(krow + lane + 32 * c, p.scale * dk[r][c]);
-            st(vrow + lane + 32 * c, dv[r][c]);
+            put(krow + lane + 32 * c, p.scale * dk[r][c], p.acc_out);
+            put(vrow + lane + 32 * c, dv[r][c], p.acc_out);
         }
     }
 }
@@ -338,25 +340,25 @@ dfa_status fwd_impl(const AttnProblem& p, const void* q, const void* k, const vo
     return e == cudaSuccess ? DFA_OK : fail(DFA_ERR_CUDA, "simt fwd launch: %s", cudaGetErrorString(e));
 }
 
-template <typename T, int D>
+template <typename T, typename OT, int D>
 dfa_status bwd_impl(const AttnProblem& p, const void* q, const void* k, const void* v,
                     const void* dO, const float* lse, const float* delta, void* dQ, void* dK,
                     void* dV, cudaStream_t s) {
     const size_t smem_q = sizeof(float) * (2 * BQ + 2 * BK) * (D + 1);
     const size_t smem_kv = sizeof(float) * ((2 * BQ + 2 * BK) * (D + 1) + 2 * BQ);
-    auto kq = simt_bwd_dq_kernel<T, D>;
-    auto kkv = simt_bwd_dkv_kernel<T, D>;
+    auto kq = simt_bwd_dq_kernel<T, OT, D>;
+    auto kkv = simt_bwd_dkv_kernel<T, OT, D>;
     if (prep(kq, smem_q) != cudaSuccess || prep(kkv, smem_kv) != cudaSuccess)
         return fail(DFA_ERR_CUDA, "simt bwd: smem attribute");
     if (p.Lq > 0) {
         dim3 gq((p.Lq + BQ - 1) / BQ, p.H, p.B);
         kq<<<gq, NWARP * 32, smem_q, s>>>(p, (const T*)q, (const T*)k, (const T*)v, (const T*)dO,
-                                          lse, delta, (T*)dQ);
+                                          lse, delta, (OT*)dQ);
     }
     if (p.Lkv > 0) {
         dim3 gkv((p.Lkv + BK - 1) / BK, p.Hkv, p.B);
         kkv<<<gkv, NWARP * 32, smem_kv, s>>>(p, (const T*)q, (const T*)k, (const T*)v,
-                                             (const T*)dO, lse, delta, (T*)dK, (T*)dV);
+                                             (const T*)dO, lse, delta, (OT*)dK, (OT*)dV);
     }
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? DFA_OK : fail(DFA_ERR_CUDA, "simt bwd launch: %s", cudaGetErrorString(e));
@@ -385,10 +387,13 @@ dfa_status simt_bwd(const AttnProblem& p, dfa_dtype dt, const void* q, const voi
     if (p.B == 0) return DFA_OK;
     using bf = __nv_bfloat16;
     if (dt == DFA_F32)
-        return p.D == 64 ? bwd_impl<float, 64>(p, q, k, v, dO, lse, delta, dQ, dK, dV, s)
-                         : bwd_impl<float, 128>(p, q, k, v, dO, lse, delta, dQ, dK, dV, s);
-    return p.D == 64 ? bwd_impl<bf, 64>(p, q, k, v, dO, lse, delta, dQ, dK, dV, s)
-                     : bwd_impl<bf, 128>(p, q, k, v, dO, lse, delta, dQ, dK, dV, s);
+        return p.D == 64 ? bwd_impl<float, float, 64>(p, q, k, v, dO, lse, delta, dQ, dK, dV, s)
+                         : bwd_impl<float, float, 128>(p, q, k, v, dO, lse, delta, dQ, dK, dV, s);
+    if (p.acc_out)
+        return p.D == 64 ? bwd_impl<bf, float, 64>(p, q, k, v, dO, lse, delta, dQ, dK, dV, s)
+                         : bwd_impl<bf, float, 128>(p, q, k, v, dO, lse, delta, dQ, dK, dV, s);
+    return p.D == 64 ? bwd_impl<bf, bf, 64>(p, q, k, v, dO, lse, delta, dQ, dK, dV, s)
+                     : bwd_impl<bf, bf, 128>(p, q, k, v, dO, lse, delta, dQ, dK, dV, s);
 }
 
 }  // namespace dfa

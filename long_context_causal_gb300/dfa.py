@@ -49,6 +49,9 @@ def _load() -> ctypes.CDLL:
         "dfa_attn_fwd": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, f32, i32, vp, vp, vp, sz, vp]),
         "dfa_attn_bwd": (i32, [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, f32, i32,
                                vp, vp, vp, vp, sz, vp]),
+        "dfa_chunk_attn_bwd": (i32, [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i64, i64, i32, f32,
+                                     vp, vp, vp, vp, sz, vp]),
+        "dfa_chunk_bwd_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
         "dfa_attn_fwd_noalloc": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, f32, i32, vp, vp, vp]),
         "dfa_check_errors": (i32, [vp]),
         "dfa_last_error": (ctypes.c_char_p, []),
@@ -133,6 +136,39 @@ def dfa_chunk_attn_fwd(q, k, v, q_offset: int = 0, kv_offset: int = 0, causal: b
                                    qs, ks, int(q_offset), int(kv_offset), int(bool(causal)), scale,
                                    _ptr(O_partial), _ptr(lse), _stream(stream)))
     return O_partial, lse
+
+
+def dfa_chunk_bwd_workspace_size(B, H, H_kv, Lq, Lkv, D) -> int:
+    return int(_lib.dfa_chunk_bwd_workspace_size(B, H, H_kv, Lq, Lkv, D))
+
+
+def dfa_chunk_attn_bwd(q, k, v, O, lse, dO, q_offset: int = 0, kv_offset: int = 0, causal: bool = True,
+                       scale: float | None = None, dQ_acc=None, dK_acc=None, dV_acc=None,
+                       workspace_buf=None, stream=None):
+    """Backward step of one (query chunk, key chunk) pair from the rows' final
+    (O, lse): adds the pair's share into fp32 accumulators (created zeroed when
+    not given) and returns (dQ_acc [B,Lq,H,D], dK_acc, dV_acc [B,Lkv,H_kv,D])."""
+    B, Lq, H, D = q.shape
+    _, Lkv, Hkv, _ = k.shape
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (O, "O"), (lse, "lse"), (dO, "dO")):
+        _dense(t, n)
+    scale = D ** -0.5 if scale is None else float(scale)
+    f32 = dict(dtype=torch.float32, device=q.device)
+    dQ_acc = torch.zeros((B, Lq, H, D), **f32) if dQ_acc is None else dQ_acc
+    dK_acc = torch.zeros((B, Lkv, Hkv, D), **f32) if dK_acc is None else dK_acc
+    dV_acc = torch.zeros((B, Lkv, Hkv, D), **f32) if dV_acc is None else dV_acc
+    for t, n in ((dQ_acc, "dQ_acc"), (dK_acc, "dK_acc"), (dV_acc, "dV_acc")):
+        _dense(t, n)
+        if t.dtype != torch.float32:
+            raise ValueError(f"{n} must be fp32")
+    if workspace_buf is None:
+        workspace_buf = torch.empty(max(dfa_chunk_bwd_workspace_size(B, H, Hkv, Lq, Lkv, D), 16),
+                                    dtype=torch.uint8, device=q.device)
+    _check(_lib.dfa_chunk_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(O), _ptr(lse), _ptr(dO), _dtype(q),
+                                   B, H, Hkv, Lq, Lkv, D, int(q_offset), int(kv_offset), int(bool(causal)),
+                                   scale, _ptr(dQ_acc), _ptr(dK_acc), _ptr(dV_acc), _ptr(workspace_buf),
+                                   workspace_buf.numel(), _stream(stream)))
+    return dQ_acc, dK_acc, dV_acc
 
 
 def dfa_merge_partials(O_a, lse_a, O_b, lse_b, O_out=None, lse_out=None, stream=None):
