@@ -43,6 +43,7 @@ def parse():
     ap.add_argument("--sched", choices=["balanced", "unbalanced"], default="balanced")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-chunk-step", action="store_true", help="skip the per-worker chunk-step timing")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target oracle sample time")
     return ap.parse_args()
 
@@ -205,6 +206,57 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+def chunk_step_timing(w, q, k, v, O, lse, do, stream, dfa, reps=5):
+    """One worker's calls of the distributed method on this workload's chunks
+    (C = S / n_chunks): the chunk step (partial O + lse) and its backward step
+    (partial dQ/dK/dV from the saved O/lse), on the last query chunk against
+    the first key chunk (no mask) and on the diagonal pair.  Reported beside
+    the headline, not part of it."""
+    import torch
+    if w.n_chunks < 2:
+        return None
+    C = w.S // w.n_chunks
+    out = {"C": C}
+    f32 = dict(dtype=torch.float32, device=q.device)
+    ws = torch.empty(max(dfa.dfa_chunk_bwd_workspace_size(w.B, w.H, w.H_kv, C, C, w.D), 16),
+                     dtype=torch.uint8, device=q.device)
+    Op = torch.empty((w.B, C, w.H, w.D), **f32)
+    lp = torch.empty((w.B, w.H, C), **f32)
+    acc = (torch.zeros((w.B, C, w.H, w.D), **f32), torch.zeros((w.B, C, w.H_kv, w.D), **f32),
+           torch.zeros((w.B, C, w.H_kv, w.D), **f32))
+    for name, (qa, ka) in (("off_diagonal", (w.S - C, 0)), ("diagonal", (w.S - C, w.S - C))):
+        qs, ks = slice(qa, qa + C), slice(ka, ka + C)
+        qc, kc, vc, dc = (t.contiguous() for t in (q[:, qs], k[:, ks], v[:, ks], do[:, qs]))
+        Oc, lc = O[:, qs].contiguous(), lse[:, :, qs].contiguous()
+
+        def fwd():
+            dfa.dfa_chunk_attn_fwd(qc, kc, vc, q_offset=qa, kv_offset=ka, scale=w.scale, O_partial=Op,
+                                   lse=lp, stream=stream)
+
+        def bwd():
+            dfa.dfa_chunk_attn_bwd(qc, kc, vc, Oc, lc, dc, q_offset=qa, kv_offset=ka, scale=w.scale,
+                                   dQ_acc=acc[0], dK_acc=acc[1], dV_acc=acc[2], workspace_buf=ws, stream=stream)
+
+        res = {}
+        for tag, fn, per_pair in (("fwd", fwd, 4), ("bwd", bwd, 10)):
+            for _ in range(2):
+                fn()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(q.device)
+            a.record(stream)
+            for _ in range(reps):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize(q.device)
+            ms = a.elapsed_time(b) / reps
+            pairs = w.B * w.H * (C * C if qa != ka else C * (C + 1) // 2)
+            res[f"{tag}_ms"] = ms
+            res[f"{tag}_tflops"] = pairs * w.D * per_pair / (ms * 1e-3) / 1e12
+        out[name] = res
+    dfa.dfa_check_errors(stream)
+    return out
+
+
 # ---------------------------------------------------------------- GPU arm
 def main():
     args = parse()
@@ -323,6 +375,8 @@ def main():
         e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": n_e2e}
 
+    chunk = None if args.no_chunk_step else chunk_step_timing(w, q, k, v, O, lse, do, stream, dfa)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         fl, el, cores, desc = oracle_sample(w, args.cpu_seconds)
@@ -349,6 +403,7 @@ def main():
         "roofline_fwd": {"bound": "tensor", "achieved": fwd_tflops, "peak": peak_tc, "unit": "TFLOP/s",
                          "frac": fwd_tflops / peak_tc},
         "cpu_baseline": cpu,
+        "chunk_step": chunk,
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clk,
