@@ -240,8 +240,11 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (lane == 0) {
             trace_count(a.trace, a.trace_cap, 6, n);
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------------------ MMA issuer
+        // One thread: tcgen05.mma / commit / fence and mbarrier waits are all
+        // per-thread, and a lone thread keeps the gaps between MMA groups short
+        // (the tensor pipe queues little ahead, so every cycle between groups is idle).
         constexpr uint32_t idS = idesc_bf16_f32(BT, BT, false, false);   // S^T, dP^T
         constexpr uint32_t idKM = idesc_bf16_f32(BT, D, false, true);    // dV, dK: B N-major
         constexpr uint32_t idQ = idesc_bf16_f32(D, BT, true, true);      // dQ^T: M = head dim
@@ -256,19 +259,15 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         bool ok = true;
         uint64_t wt[4] = {0, 0, 0, 0};   // inputs (Q, dO, K/V, dK/dV free), dq_free, P^T, dS^T
         auto wait = [&](uint64_t* bar, uint32_t parity, int slot) {
-            ok = ok && __all_sync(0xffffffffu,
-                                  mbar_wait_acc(bar, parity, abort_flag, a.err, a.trace ? &wt[slot] : nullptr));
+            ok = ok && mbar_wait_acc(bar, parity, abort_flag, a.err, a.trace ? &wt[slot] : nullptr);
             if (ok) tc_fence_after();
             return ok;
         };
-        auto commit = [&](uint64_t* bar) {
-            if (lane == 0) mma_commit(bar);
-            __syncwarp();
-        };
+        auto commit = [&](uint64_t* bar) { mma_commit(bar); };
         auto issue_S = [&](uint32_t m) {   // S^T(m) = K Q_m^T
             const uint32_t s = m & 1;
             if (!wait(&q_full[s], (m >> 1) & 1, 0)) return false;
-            if (lane == 0) {
+            {
                 const uint64_t b0 = dQk + s * kSlot;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + kColS, dKk + kmaj(kk), b0 + kmaj(kk), idS, kk > 0);
@@ -280,7 +279,7 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const uint32_t s = m & 1;
             if (!wait(&do_full[s], (m >> 1) & 1, 0)) return false;
             if (m > 0 && !wait(dq_free, (m - 1) & 1, 1)) return false;
-            if (lane == 0) {
+            {
                 const uint64_t b0 = dOk + s * kSlot;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + kColDP, dVk + kmaj(kk), b0 + kmaj(kk), idS, kk > 0);
@@ -299,7 +298,7 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 if (k == 0 && !wait(kd_empty, (kvi & 1) ^ 1, 0)) break;
                 if (!wait(p_done, n & 1, 2)) break;
                 const uint32_t acc0 = k > 0 ? 1u : 0u;
-                if (lane == 0) {   // dV += P^T dO: P^T of query half h at S + 64h
+                {   // dV += P^T dO: P^T of query half h at S + 64h
                     const uint64_t b0 = dOn + s * kSlot;
 #pragma unroll
                     for (int kk = 0; kk < BT / 16; ++kk)
@@ -309,13 +308,13 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 commit(&do_empty[s]);
                 if (more && !issue_S(n + 1)) break;       // S^T columns are free after phase 1
                 if (!wait(ds_done, n & 1, 3)) break;
-                if (lane == 0) {   // dQ^T = K^T dS^T into the dP^T columns; drained while dK runs
+                {   // dQ^T = K^T dS^T into the dP^T columns; drained while dK runs
 #pragma unroll
                     for (int kk = 0; kk < BT / 16; ++kk)
                         mma_ss(tmem + kColDP, dKn + kk * kRows16, dSn + kk * kRows16, idQ, kk > 0);
                 }
                 commit(dq_full);
-                if (lane == 0) {   // dK += dS^T Q
+                {   // dK += dS^T Q
                     const uint64_t bq = dQn + s * kSlot;
 #pragma unroll
                     for (int kk = 0; kk < BT / 16; ++kk)
@@ -335,7 +334,7 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         commit(done);
         int dummy = 0;
         mbar_wait(done, 0, &dummy, a.err);
-        if (lane == 0) {
+        {
             trace_count(a.trace, a.trace_cap, 4, n);
             for (int z = 0; z < 4; ++z) trace_wait(a.trace, a.trace_cap, 1 + z, wt[z]);
         }

@@ -248,8 +248,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             if (qi_issued > 0) mbar_wait(q_full, (qi_issued - 1) & 1, &dummy, nullptr);
         }
         if (lane == 0) trace_count(a.trace, a.trace_cap, 6, ld / 2);
-    } else if (warp == 1) {
+    } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------------------ MMA issuer
+        // One thread: MMAs, commits, fences and mbarrier waits are per-thread, and a
+        // lone thread keeps the gaps between MMA groups (idle tensor-pipe time) short.
         const uint32_t idS = idesc_bf16_f32(BM, BN, false, false);
         const uint32_t idO = idesc_bf16_f32(BM, D, false, true);
         // Descriptors are built once and advanced by adding (byte offset / 16):
@@ -263,7 +265,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         uint32_t cons = 0, t = 0, qi = 0;
         bool ok = true;
         auto issue_S = [&](int w, uint32_t slot) {
-            if (lane == 0) {
+            {
                 const uint64_t a0 = dQk + w * kSlotStep, b0 = dKk + slot * kSlotStep;
                 const uint32_t d = tmem + w * 128;
 #pragma unroll
@@ -274,7 +276,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             }
         };
         auto issue_PV = [&](int w, uint32_t slot, bool acc) {
-            if (lane == 0) {
+            {
                 const uint64_t b0 = dVn + slot * kSlotStep;
                 const uint32_t d = tmem + 256 + w * 128, a = tmem + w * 128;
                 mma_ts(d, a, b0, idO, acc ? 1u : 0u);
@@ -283,14 +285,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             }
         };
         auto wait = [&](uint64_t* bar, uint32_t parity) {
-            ok = ok && __all_sync(0xffffffffu, mbar_wait_acc(bar, parity, abort_flag, a.err, nullptr));
+            ok = ok && mbar_wait_acc(bar, parity, abort_flag, a.err, nullptr);
             if (ok) tc_fence_after();
             return ok;
         };
-        auto commit = [&](uint64_t* bar) {
-            if (lane == 0) mma_commit(bar);
-            __syncwarp();
-        };
+        auto commit = [&](uint64_t* bar) { mma_commit(bar); };
         for (int it = it_begin; it < it_end && ok; ++it) {
             const Item x = decode(a, a.wl_items ? a.wl_items[it] : it);
             if (x.n_kv == 0) continue;
@@ -335,7 +334,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         commit(done);
         int dummy = 0;
         mbar_wait(done, 0, &dummy, a.err);
-        if (lane == 0) trace_count(a.trace, a.trace_cap, 4, t);
+        trace_count(a.trace, a.trace_cap, 4, t);
     } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax warpgroups
         const int w = (warp - 4) / 4;                 // which query tile
