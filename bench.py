@@ -111,18 +111,33 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(self.rows)}
 
 
-def dist_setup(n_gpus):
+def dist_setup(n_gpus, backend="nccl"):
+    """One process per GPU (torchrun sets RANK/LOCAL_RANK/WORLD_SIZE/MASTER_*).
+    backend "gloo" runs the same rank logic on CPU (tests)."""
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group(backend)
+    elif backend == "nccl":
         torch.cuda.set_device(0)
     return rank, world, local
+
+
+def rank_seed(base_seed, rank):
+    """Weak scaling: every rank draws its own independent copy of the workload."""
+    return base_seed + rank
+
+
+def job_value(flops_per_rank, ms_per_step, world):
+    """Whole-job throughput (TFLOP/s): all ranks' work over the slowest rank's time."""
+    return world * flops_per_rank / (ms_per_step * 1e-3) / 1e12
 
 
 def barrier(world):
@@ -131,12 +146,12 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(x, world):
+def max_over_ranks(x, world, device="cuda"):
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -278,7 +293,7 @@ def main():
 
     rank, world, local = dist_setup(args.gpus)
     dev = torch.device("cuda", local if world > 1 else 0)
-    seed = w.seed + rank
+    seed = rank_seed(w.seed, rank)
     q, k, v, do = make(w.B, w.H, w.H_kv, w.S, w.D, w.dtype, seed=seed, device=dev, k_scale=w.k_scale)
     O = torch.empty_like(q)
     lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
@@ -328,7 +343,7 @@ def main():
     bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     flops = w.causal_flops()
     ms_step = total_ms / args.steps
-    value = world * flops / (ms_step * 1e-3) / 1e12
+    value = job_value(flops, ms_step, world)
 
     peaks, peak_kind = measured_peaks()
     peak_tc = float(peaks["bf16_tflops"])
@@ -372,7 +387,7 @@ def main():
         torch.cuda.synchronize(dev)
         barrier(world)
         e2e_ms = max_over_ranks(a.elapsed_time(b), world) / n_e2e
-        e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": job_value(flops, e2e_ms, world), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": n_e2e}
 
     chunk = None if args.no_chunk_step else chunk_step_timing(w, q, k, v, O, lse, do, stream, dfa)
