@@ -285,7 +285,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             }
         };
         auto wait = [&](uint64_t* bar, uint32_t parity) {
-            ok = ok && mbar_wait_acc(bar, parity, abort_flag, a.err, nullptr);
+            ok = ok && mbar_wait_issuer(bar, parity, abort_flag, a.err);
             if (ok) tc_fence_after();
             return ok;
         };

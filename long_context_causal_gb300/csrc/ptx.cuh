@@ -119,6 +119,26 @@ static __device__ __noinline__ bool mbar_wait_traced(uint64_t* bar, uint32_t par
     *acc_cycles += clock64() - t0;
     return ok;
 }
+// Non-blocking test of a phase (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Wait for the MMA issuer: a plain test first (the common case is a phase that
+// has already completed, and a potentially-suspending try_wait there leaves the
+// tensor pipe idle for hundreds of cycles), then the bounded blocking wait.
+__device__ __forceinline__ bool mbar_wait_issuer(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                 int* err) {
+    if (mbar_test_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, abort_flag, err);
+}
 __device__ __forceinline__ bool mbar_wait_acc(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                               int* err, uint64_t* acc_cycles) {
     if (acc_cycles) return mbar_wait_traced(bar, parity, abort_flag, err, acc_cycles);
