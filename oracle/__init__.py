@@ -61,11 +61,14 @@ def _load():
             lib.oracle_dq_rows.argtypes = [_DP, _DP, _DP, _DP] + dims + [_LP, _I64, _DP, ctypes.c_int]
             lib.oracle_dkv_rows.argtypes = [_DP, _DP, _DP, _DP] + dims + [_LP, _I64, _DP, _DP, ctypes.c_int]
             lib.oracle_merge.argtypes = [_DP, _DP, _DP, _DP, _I64, _I64, _I64, _I64, _DP, _DP]
+            local = [_I64] * 8 + [ctypes.c_double, _I64, _I64]
+            lib.oracle_fwd_local.argtypes = [_DP, _DP, _DP] + local + [_DP, _DP, ctypes.c_int]
+            lib.oracle_bwd_local.argtypes = [_DP, _DP, _DP, _DP] + local + [_DP, _DP, _DP, ctypes.c_int]
             lib.oracle_delta.argtypes = [_DP, _DP, _DP, _DP] + dims + [_DP, ctypes.c_int]
             lib.oracle_chunk_bwd.argtypes = [_DP, _DP, _DP, _DP, _DP, _DP] + dims + [_DP, _DP, _DP, ctypes.c_int]
             for f in ("oracle_fwd", "oracle_fwd_rows", "oracle_bwd", "oracle_dq_rows",
                       "oracle_dkv_rows", "oracle_merge", "oracle_num_threads", "oracle_delta",
-                      "oracle_chunk_bwd"):
+                      "oracle_chunk_bwd", "oracle_fwd_local", "oracle_bwd_local"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -167,6 +170,32 @@ def attn_dkv_rows(q, k, v, dO, krows, *, causal=True, scale=None, q_offset=0, kv
                                  _p(dK), _p(dV), int(threads))
     _check(rc, "dkv_rows")
     return dK, dV
+
+
+def attn_fwd_local(q, k, v, *, chunk, window, scale=None, q_offset=0, kv_offset=0, threads=0):
+    """Causal forward where a query sees only its own chunk (chunk tokens long,
+    positions counted from 0) and the window - 1 chunks before it."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, Hkv, Lq, Lkv, D = _dims(q, k)
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    O = np.empty_like(q)
+    lse = np.empty((B, H, Lq))
+    rc = _load().oracle_fwd_local(_p(q), _p(k), _p(v), B, H, Hkv, Lq, Lkv, D, q_offset, kv_offset, scale,
+                                  int(chunk), int(window), _p(O), _p(lse), int(threads))
+    _check(rc, "fwd_local")
+    return O, lse
+
+
+def attn_bwd_local(q, k, v, dO, *, chunk, window, scale=None, q_offset=0, kv_offset=0, threads=0):
+    """dQ, dK, dV of attn_fwd_local."""
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    B, H, Hkv, Lq, Lkv, D = _dims(q, k)
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    dQ, dK, dV = np.empty_like(q), np.empty_like(k), np.empty_like(v)
+    rc = _load().oracle_bwd_local(_p(q), _p(k), _p(v), _p(dO), B, H, Hkv, Lq, Lkv, D, q_offset, kv_offset,
+                                  scale, int(chunk), int(window), _p(dQ), _p(dK), _p(dV), int(threads))
+    _check(rc, "bwd_local")
+    return dQ, dK, dV
 
 
 def delta(q, k, v, dO, *, causal=True, scale=None, q_offset=0, kv_offset=0, threads=0):

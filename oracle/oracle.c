@@ -27,6 +27,10 @@
  *   Delta_i = sum_j P_ij dP_ij            (the explicit definition, not dO.O)
  *   dS_ij = P_ij (dP_ij - Delta_i)
  *   dQ_i  = scale sum_j dS_ij k_j,   dK_j = scale sum_i dS_ij q_i
+ * The local sliding window of App. F (a worker attends only to its own chunk
+ * and the neighbouring ones before it) is read as: key position kp is visible
+ * from query position qp iff kp <= qp and floor(kp / C) >= floor(qp / C) - (w - 1)
+ * for chunk length C and a window of w chunks (oracle_fwd_local/_bwd_local).
  * A worker's backward step for one (query chunk, key chunk) pair (§3.3) uses
  * the rows' global lse_i and Delta_i and gives the pair's share of dQ (for the
  * query chunk) and of dK, dV (for the key chunk); summed over the pairs these
@@ -51,6 +55,7 @@ typedef struct {
     int64_t B, H, Hkv, Lq, Lkv, D, q_offset, kv_offset;
     int causal;
     double scale;
+    int64_t win_c, win_w;   /* local window: chunk length and chunks per window (0: none) */
 } dims_t;
 
 static inline const double* qrow(const double* q, const dims_t* d, int64_t b, int64_t i, int64_t h) {
@@ -59,8 +64,15 @@ static inline const double* qrow(const double* q, const dims_t* d, int64_t b, in
 static inline const double* kvrow(const double* k, const dims_t* d, int64_t b, int64_t j, int64_t g) {
     return k + ((b * d->Lkv + j) * d->Hkv + g) * d->D;
 }
+/* Causal visibility; with a local window (DISTFLASHATTN App. F: a worker
+ * attends only to its own and the neighbouring chunks) a key must also lie in
+ * the query's chunk or one of the win_w - 1 chunks before it. */
 static inline int visible(const dims_t* d, int64_t i, int64_t j) {
-    return !d->causal || (d->kv_offset + j) <= (d->q_offset + i);
+    const int64_t qp = d->q_offset + i, kp = d->kv_offset + j;
+    if (!d->causal) return 1;
+    if (kp > qp) return 0;
+    if (d->win_w > 0 && kp / d->win_c < qp / d->win_c - (d->win_w - 1)) return 0;
+    return 1;
 }
 
 /* One full score row s[0..Lkv) for query (b, h, i); masked keys get -inf.
@@ -129,11 +141,9 @@ int oracle_num_threads(void) {
 }
 
 /* Full forward over every (b, h, i). */
-int oracle_fwd(const double* q, const double* k, const double* v,
-               int64_t B, int64_t H, int64_t Hkv, int64_t Lq, int64_t Lkv, int64_t D,
-               int64_t q_offset, int64_t kv_offset, int causal, double scale,
-               double* O, double* lse, int nthreads) {
-    dims_t d = {B, H, Hkv, Lq, Lkv, D, q_offset, kv_offset, causal, scale};
+static int fwd_all(const double* q, const double* k, const double* v, dims_t d,
+                   double* O, double* lse, int nthreads) {
+    const int64_t B = d.B, H = d.H, Lq = d.Lq, Lkv = d.Lkv, D = d.D;
     if (check_dims(&d)) return 1;
     set_threads(nthreads);
     const int64_t total = B * H * Lq;
@@ -155,6 +165,24 @@ int oracle_fwd(const double* q, const double* k, const double* v,
         }
     }
     return err;
+}
+
+int oracle_fwd(const double* q, const double* k, const double* v,
+               int64_t B, int64_t H, int64_t Hkv, int64_t Lq, int64_t Lkv, int64_t D,
+               int64_t q_offset, int64_t kv_offset, int causal, double scale,
+               double* O, double* lse, int nthreads) {
+    dims_t d = {B, H, Hkv, Lq, Lkv, D, q_offset, kv_offset, causal, scale, 0, 0};
+    return fwd_all(q, k, v, d, O, lse, nthreads);
+}
+
+/* Causal forward restricted to a local window of win_w chunks of win_c tokens. */
+int oracle_fwd_local(const double* q, const double* k, const double* v,
+                     int64_t B, int64_t H, int64_t Hkv, int64_t Lq, int64_t Lkv, int64_t D,
+                     int64_t q_offset, int64_t kv_offset, double scale, int64_t win_c, int64_t win_w,
+                     double* O, double* lse, int nthreads) {
+    if (win_c <= 0 || win_w <= 0) return 1;
+    dims_t d = {B, H, Hkv, Lq, Lkv, D, q_offset, kv_offset, 1, scale, win_c, win_w};
+    return fwd_all(q, k, v, d, O, lse, nthreads);
 }
 
 /* Forward on selected rows: rows is [n, 3] of (b, h, i); O_rows [n, D], lse_rows [n]. */
@@ -206,11 +234,10 @@ static void bwd_row(const double* q, const double* k, const double* v, const dou
 }
 
 /* Full backward.  dK/dV are accumulated per thread and reduced at the end. */
-int oracle_bwd(const double* q, const double* k, const double* v, const double* dO,
-               int64_t B, int64_t H, int64_t Hkv, int64_t Lq, int64_t Lkv, int64_t D,
-               int64_t q_offset, int64_t kv_offset, int causal, double scale,
-               double* dQ, double* dK, double* dV, int nthreads) {
-    dims_t d = {B, H, Hkv, Lq, Lkv, D, q_offset, kv_offset, causal, scale};
+static int bwd_all(const double* q, const double* k, const double* v, const double* dO, dims_t d,
+                   double* dQ, double* dK, double* dV, int nthreads) {
+    const int64_t B = d.B, H = d.H, Hkv = d.Hkv, Lq = d.Lq, Lkv = d.Lkv, D = d.D;
+    const double scale = d.scale;
     if (check_dims(&d)) return 1;
     set_threads(nthreads);
     const int64_t kvn = B * Lkv * Hkv * D;
@@ -257,6 +284,24 @@ int oracle_bwd(const double* q, const double* k, const double* v, const double* 
         free(p); free(ds); free(lk); free(lv);
     }
     return err;
+}
+
+int oracle_bwd(const double* q, const double* k, const double* v, const double* dO,
+               int64_t B, int64_t H, int64_t Hkv, int64_t Lq, int64_t Lkv, int64_t D,
+               int64_t q_offset, int64_t kv_offset, int causal, double scale,
+               double* dQ, double* dK, double* dV, int nthreads) {
+    dims_t d = {B, H, Hkv, Lq, Lkv, D, q_offset, kv_offset, causal, scale, 0, 0};
+    return bwd_all(q, k, v, dO, d, dQ, dK, dV, nthreads);
+}
+
+/* Backward of oracle_fwd_local. */
+int oracle_bwd_local(const double* q, const double* k, const double* v, const double* dO,
+                     int64_t B, int64_t H, int64_t Hkv, int64_t Lq, int64_t Lkv, int64_t D,
+                     int64_t q_offset, int64_t kv_offset, double scale, int64_t win_c, int64_t win_w,
+                     double* dQ, double* dK, double* dV, int nthreads) {
+    if (win_c <= 0 || win_w <= 0) return 1;
+    dims_t d = {B, H, Hkv, Lq, Lkv, D, q_offset, kv_offset, 1, scale, win_c, win_w};
+    return bwd_all(q, k, v, dO, d, dQ, dK, dV, nthreads);
 }
 
 /* dQ on selected query rows (row-local): rows [n,3] of (b, h, i); dQ_rows [n, D]. */

@@ -207,6 +207,68 @@ def test_chunk_pair_above_the_diagonal_contributes_nothing():
     assert np.all(pq[0, 2, 1] == 0.0)
 
 
+# ---------------------------------------------------------------- local window (App. F)
+def test_window_covering_every_chunk_is_plain_causal():
+    B, H, Hkv, S, D = 1, 2, 1, 12, 3
+    q, k, v, dO = rnd((B, S, H, D), 400), rnd((B, S, Hkv, D), 401), rnd((B, S, Hkv, D), 402), rnd((B, S, H, D), 403)
+    for w in (3, 4, 7):
+        a, b = oracle.attn_fwd_local(q, k, v, chunk=4, window=w), oracle.attn_fwd(q, k, v)
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+        for x, y in zip(oracle.attn_bwd_local(q, k, v, dO, chunk=4, window=w), oracle.attn_bwd(q, k, v, dO)):
+            assert np.array_equal(x, y)
+
+
+def test_window_of_one_chunk_is_independent_chunks():
+    B, H, Hkv, S, D, C = 2, 2, 2, 15, 3, 5
+    q, k, v, dO = rnd((B, S, H, D), 410), rnd((B, S, Hkv, D), 411), rnd((B, S, Hkv, D), 412), rnd((B, S, H, D), 413)
+    O, lse = oracle.attn_fwd_local(q, k, v, chunk=C, window=1)
+    dQ, dK, dV = oracle.attn_bwd_local(q, k, v, dO, chunk=C, window=1)
+    for c in range(S // C):
+        sl = slice(c * C, (c + 1) * C)
+        Oc, lc = oracle.attn_fwd(q[:, sl], k[:, sl], v[:, sl])
+        np.testing.assert_allclose(O[:, sl], Oc, atol=1e-14)
+        np.testing.assert_allclose(lse[:, :, sl], lc, atol=1e-14)
+        for g, r in zip((dQ[:, sl], dK[:, sl], dV[:, sl]), oracle.attn_bwd(q[:, sl], k[:, sl], v[:, sl], dO[:, sl])):
+            np.testing.assert_allclose(g, r, atol=1e-13)
+
+
+def test_window_of_two_chunks_merges_the_neighbour():
+    # the pages' recipe: a worker fetches only the previous worker's key/value
+    # block and merges that partial with its own chunk's (§3.2 merge rule)
+    B, H, Hkv, S, D, C = 1, 2, 1, 18, 4, 6
+    q, k, v = rnd((B, S, H, D), 420), rnd((B, S, Hkv, D), 421), rnd((B, S, Hkv, D), 422)
+    O, lse = oracle.attn_fwd_local(q, k, v, chunk=C, window=2)
+    for p in range(S // C):
+        qs = slice(p * C, (p + 1) * C)
+        acc = oracle.attn_fwd(q[:, qs], k[:, qs], v[:, qs], q_offset=p * C, kv_offset=p * C)
+        if p > 0:
+            ks = slice((p - 1) * C, p * C)
+            acc = oracle.merge(*acc, *oracle.attn_fwd(q[:, qs], k[:, ks], v[:, ks], q_offset=p * C,
+                                                      kv_offset=(p - 1) * C))
+        np.testing.assert_allclose(O[:, qs], acc[0], atol=1e-13)
+        np.testing.assert_allclose(lse[:, :, qs], acc[1], atol=1e-13)
+
+
+def test_window_gradients_match_finite_differences():
+    B, H, Hkv, S, D, C, w = 1, 2, 1, 9, 3, 3, 2
+    q, k, v, dO = rnd((B, S, H, D), 430), rnd((B, S, Hkv, D), 431), rnd((B, S, Hkv, D), 432), rnd((B, S, H, D), 433)
+    dQ, dK, dV = oracle.attn_bwd_local(q, k, v, dO, chunk=C, window=w, scale=0.8)
+    loss = lambda q_, k_, v_: float(np.sum(oracle.attn_fwd_local(q_, k_, v_, chunk=C, window=w, scale=0.8)[0] * dO))
+    h = 1e-6
+    for idx, x, g in (("q", q, dQ), ("k", k, dK), ("v", v, dV)):
+        fd = np.zeros_like(x)
+        it = np.nditer(x, flags=["multi_index"])
+        for _ in it:
+            m = it.multi_index
+            xp, xm = x.copy(), x.copy()
+            xp[m] += h
+            xm[m] -= h
+            args_p = {"q": q, "k": k, "v": v}; args_p[idx] = xp
+            args_m = {"q": q, "k": k, "v": v}; args_m[idx] = xm
+            fd[m] = (loss(args_p["q"], args_p["k"], args_p["v"]) - loss(args_m["q"], args_m["k"], args_m["v"])) / (2 * h)
+        assert np.max(np.abs(fd - g) / np.maximum(1.0, np.abs(g))) < 1e-7, idx
+
+
 def test_merge_neutral_element_and_symmetry():
     O_a, O_b = rnd((1, 3, 2, 4), 80), rnd((1, 3, 2, 4), 81)
     la, lb = rnd((1, 2, 3), 82), rnd((1, 2, 3), 83)
