@@ -150,6 +150,24 @@ dfa_status dfa_attn_bwd(const void* q, const void* k, const void* v, const void*
                         float scale, dfa_sched sched, void* dQ, void* dK, void* dV,
                         void* workspace, size_t ws_bytes, void* stream);
 
+/* Local sliding window (DISTFLASHATTN App. F: with a local window each worker
+ * attends only to its own chunk and the neighbouring chunks before it, and
+ * fetches only those key/value blocks).  Causal attention in which a query at
+ * position qp sees key kp only if kp <= qp and kp / C >= qp / C - (window - 1),
+ * C = S / n_chunks the chunk length; window >= n_chunks is plain causal.
+ * Arguments, layouts, workspace and errors as dfa_attn_fwd / dfa_attn_bwd
+ * (causal implied); INVALID_ARG for window < 1.  Key/value tiles entirely
+ * outside a query tile's window are not loaded or computed. */
+dfa_status dfa_attn_fwd_local(const void* q, const void* k, const void* v, dfa_dtype dt,
+                              int B, int H, int H_kv, int S, int D, int n_chunks, int window,
+                              float scale, dfa_sched sched, void* O, float* lse,
+                              void* workspace, size_t ws_bytes, void* stream);
+dfa_status dfa_attn_bwd_local(const void* q, const void* k, const void* v, const void* O,
+                              const float* lse, const void* dO, dfa_dtype dt,
+                              int B, int H, int H_kv, int S, int D, int n_chunks, int window,
+                              float scale, dfa_sched sched, void* dQ, void* dK, void* dV,
+                              void* workspace, size_t ws_bytes, void* stream);
+
 /* dfa_attn_fwd for callers that cannot allocate device memory.  The paper
  * has no counterpart to this entry point.  Some callers cannot call
  * cudaMalloc where they run attention: a plugin whose host framework owns

@@ -61,6 +61,9 @@ constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384;
 struct Args {
     int B, H, Hkv, Lq, Lkv, S_pad, causal;
     int rel;                      // kv_offset - q_offset (a multiple of 128)
+    int64_t q_off, kv_off;        // absolute positions of the first query and key row
+    int64_t win_c;                // local window: chunk length ...
+    int win_w;                    // ... and chunks per window (0: none)
     int acc_f32;                  // dK/dV: fp32 accumulate (+=) instead of bf16 store
     float scale, c2;
     const float* lse2;
@@ -85,13 +88,13 @@ struct Args {
 // on distinct tiles of a window of about 150 tiles.  Any order is correct:
 // dK/dV accumulate and the dQ reductions commute.
 struct Item {
-    int b, g, t, i0, n_q, ntiles;   // ntiles: 128-row query tiles over all heads of the group
+    int b, g, t, i0, i1, n_q, ntiles;   // query tiles [i0, i1) per head; ntiles over the group's heads
     bool down;                      // sweep query tiles from the last one down
     // k-th tile of the item: head h of the group, query tile i
     __device__ __forceinline__ void tile(int k, int G, int& h, int& i) const {
-        const int len = n_q - i0, r = k % len;
+        const int len = i1 - i0, r = k % len;
         h = g * G + k / len;
-        i = down ? n_q - 1 - r : i0 + r;
+        i = down ? i1 - 1 - r : i0 + r;
     }
 };
 
@@ -104,7 +107,15 @@ __device__ __forceinline__ Item decode(const Args& a, int it) {
     x.n_q = (a.Lq + BT - 1) / BT;
     // first query tile that sees any key of tile t: q_offset + 128 i + 127 >= kv_offset + 128 t
     x.i0 = a.causal ? min(max(x.t + a.rel / BT, 0), x.n_q) : 0;
-    x.ntiles = (a.H / a.Hkv) * (x.n_q - x.i0);
+    x.i1 = x.n_q;
+    if (a.win_w > 0) {   // local window: queries below q_hi of the tile's last key may see it
+        const int64_t kp = a.kv_off + (int64_t)x.t * BT + BT - 1;
+        const int64_t q_hi = (kp / a.win_c + a.win_w) * a.win_c - a.q_off;
+        int64_t i1 = q_hi <= 0 ? 0 : (q_hi + BT - 1) / BT;
+        if (i1 > x.n_q) i1 = x.n_q;
+        x.i1 = i1 < x.i0 ? x.i0 : (int)i1;
+    }
+    x.ntiles = (a.H / a.Hkv) * (x.i1 - x.i0);
     x.down = 2 * x.t >= a.n_units;
     return x;
 }
@@ -360,6 +371,11 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             if (x.ntiles == 0) continue;   // key tile entirely above the diagonal: nothing to do
             const int kvg = x.t * BT + r;
             const bool row_ok = kvg < a.Lkv;
+            // local window: this key is seen by queries below q_hi (chunk-relative);
+            // q_hi_tile is the lowest such bound over the tile's keys
+            const int64_t q_hi = a.win_w > 0 ? ((a.kv_off + kvg) / a.win_c + a.win_w) * a.win_c - a.q_off : INT64_MAX;
+            const int64_t q_hi_tile =
+                a.win_w > 0 ? ((a.kv_off + (int64_t)x.t * BT) / a.win_c + a.win_w) * a.win_c - a.q_off : INT64_MAX;
             for (int k = 0; k < x.ntiles; ++k, ++n) {
                 int h, i;
                 x.tile(k, G, h, i);
@@ -373,6 +389,7 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 // Elements outside the causal triangle or the sequence only occur on
                 // the diagonal tile and on ragged edges; elsewhere no mask is applied.
                 const bool full = !(a.causal && i == x.t + a.rel / BT) && (i + 1) * BT <= a.Lq &&
+                                  (int64_t)(i + 1) * BT <= q_hi_tile &&
                                   (x.t + 1) * BT <= a.Lkv;
                 // ---- phase 1: P^T = exp2(S^T c - lse2) -> TMEM (bf16) and registers
                 uint32_t u[32], pk[32];
@@ -383,7 +400,8 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
                         for (int z = 0; z < 32; ++z) {
                             const int qg = q0 + c + z;
-                            if (!(row_ok && qg < a.Lq && !(a.causal && kvg + a.rel > qg))) u[z] = 0xff800000u;
+                            if (!(row_ok && qg < a.Lq && !(a.causal && kvg + a.rel > qg) && qg < q_hi))
+                                u[z] = 0xff800000u;
                         }
                     }
 #pragma unroll
@@ -560,6 +578,7 @@ dfa_status tc_bwd_pipelined(const AttnProblem& p, const void* q, const void* k, 
     Args a{};
     a.B = p.B; a.H = p.H; a.Hkv = p.Hkv; a.Lq = p.Lq; a.Lkv = p.Lkv; a.S_pad = S_pad; a.causal = p.causal;
     a.rel = (int)rel; a.acc_f32 = acc_f32;
+    a.q_off = p.q_offset; a.kv_off = p.kv_offset; a.win_c = p.win_c; a.win_w = p.causal ? p.win_w : 0;
     a.scale = p.scale; a.c2 = p.scale * 1.4426950408889634f;
     a.lse2 = lse2; a.delta = delta; a.dq_acc = dq_acc;
     a.dK = dK;

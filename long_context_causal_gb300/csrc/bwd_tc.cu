@@ -64,6 +64,8 @@ static_assert(BCfg<128>::kSmem <= 232448, "backward shared memory");
 
 struct BwdArgs {
     int B, H, Hkv, S, S_pad, causal;
+    int64_t win_c;                // local window: chunk length ...
+    int win_w;                    // ... and chunks per window (0: none)
     float scale, c2;              // c2 = scale * log2(e)
     const float* lse2;            // [B, H, S_pad]  lse * log2(e)
     const float* delta;           // [B, H, S_pad]
@@ -87,13 +89,13 @@ struct BwdArgs {
 // on distinct tiles of a window of about 150 tiles.  Any order is correct:
 // dK/dV accumulate and the dQ reductions commute.
 struct BItem {
-    int b, g, t, i0, n_q, ntiles;
+    int b, g, t, i0, i1, n_q, ntiles;   // query tiles [i0, i1) per head
     bool down;                      // sweep query tiles from the last one down
     // k-th tile of the item: head hh of the group (0..G-1), query tile i
     __device__ __forceinline__ void tile(int k, int& hh, int& i) const {
-        const int len = n_q - i0, r = k % len;
+        const int len = i1 - i0, r = k % len;
         hh = k / len;
-        i = down ? n_q - 1 - r : i0 + r;
+        i = down ? i1 - 1 - r : i0 + r;
     }
 };
 
@@ -105,7 +107,14 @@ __device__ __forceinline__ BItem bdecode(const BwdArgs& a, int it) {
     x.t = a.n_units - 1 - unit;          // unit u costs u + 1 query tiles per head
     x.n_q = (a.S + BT - 1) / BT;
     x.i0 = a.causal ? x.t : 0;
-    x.ntiles = (a.H / a.Hkv) * (x.n_q - x.i0);
+    x.i1 = x.n_q;
+    if (a.win_w > 0) {   // local window: queries below q_hi of the tile's last key may see it
+        const int64_t q_hi = (((int64_t)x.t * BT + BT - 1) / a.win_c + a.win_w) * a.win_c;
+        int64_t i1 = (q_hi + BT - 1) / BT;
+        if (i1 > x.n_q) i1 = x.n_q;
+        x.i1 = i1 < x.i0 ? x.i0 : (int)i1;
+    }
+    x.ntiles = (a.H / a.Hkv) * (x.i1 - x.i0);
     x.down = 2 * x.t >= a.n_units;
     return x;
 }
@@ -360,6 +369,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             const BItem x = bdecode(a, a.wl_items[it]);
             const int kvg = x.t * BT + r;                   // global key index of this thread's row
             const bool row_ok = kvg < a.S;
+            const int64_t q_hi = a.win_w > 0 ? ((int64_t)kvg / a.win_c + a.win_w) * a.win_c : INT64_MAX;
             for (int k = 0; k < x.ntiles; ++k, ++n) {
                 int hh, i;
                 x.tile(k, hh, i);
@@ -383,7 +393,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 #pragma unroll
                         for (int z = 0; z < 4; ++z) {
                             const int qg = q0 + c * 32 + e + z;
-                            const bool vis = row_ok && qg < a.S && !(a.causal && kvg > qg);
+                            const bool vis = row_ok && qg < a.S && !(a.causal && kvg > qg) && qg < q_hi;
                             const float p = vis ? ex2(fmaf(__uint_as_float(us[e + z]), a.c2, -lv[z])) : 0.f;
                             pp[z] = p;
                             dd[z] = p * (__uint_as_float(ud[e + z]) - dv[z]);
@@ -514,6 +524,7 @@ dfa_status launch(const AttnProblem& p, const void* q, const void* k, const void
         return fail(DFA_ERR_CUDA, "tensor map encoding failed");
     BwdArgs a{};
     a.B = p.B; a.H = p.H; a.Hkv = p.Hkv; a.S = p.Lq; a.S_pad = S_pad; a.causal = p.causal;
+    a.win_c = p.win_c; a.win_w = p.causal ? p.win_w : 0;
     a.scale = p.scale; a.c2 = p.scale * 1.4426950408889634f;
     a.lse2 = lse2; a.delta = delta; a.dq_acc = dq_acc;
     a.dK = static_cast<__nv_bfloat16*>(dK);

@@ -263,8 +263,13 @@ static dfa_status check_whole(dfa_dtype dt, int B, int H, int H_kv, int S, int D
     return DFA_OK;
 }
 
-static AttnProblem whole_problem(int B, int H, int H_kv, int S, int D, int causal, float scale) {
+static AttnProblem whole_problem(int B, int H, int H_kv, int S, int D, int causal, float scale,
+                                 int n_chunks = 1, int window = 0) {
     AttnProblem p{};
+    if (window > 0) {
+        p.win_c = S / n_chunks;
+        p.win_w = window;
+    }
     p.B = B; p.H = H; p.Hkv = H_kv; p.Lq = S; p.Lkv = S; p.D = D;
     p.q_sb = (int64_t)S * H * D; p.q_ss = (int64_t)H * D; p.q_sh = D;
     p.kv_sb = (int64_t)S * H_kv * D; p.kv_ss = (int64_t)H_kv * D; p.kv_sh = D;
@@ -272,15 +277,21 @@ static AttnProblem whole_problem(int B, int H, int H_kv, int S, int D, int causa
     return p;
 }
 
-extern "C" dfa_status dfa_attn_fwd(const void* q, const void* k, const void* v, dfa_dtype dt, int B, int H,
-                                   int H_kv, int S, int D, int n_chunks, int causal, float scale,
-                                   dfa_sched sched, void* O, float* lse, void* workspace, size_t ws_bytes,
-                                   void* stream) {
+static dfa_status check_window(int causal, int window) {
+    if (window < 1) return fail(DFA_ERR_INVALID_ARG, "window must be at least one chunk (got %d)", window);
+    if (!causal) return fail(DFA_ERR_INVALID_ARG, "a local window needs causal attention");
+    return DFA_OK;
+}
+
+static dfa_status attn_fwd_impl(const void* q, const void* k, const void* v, dfa_dtype dt, int B, int H,
+                                int H_kv, int S, int D, int n_chunks, int causal, int window, float scale,
+                                dfa_sched sched, void* O, float* lse, void* workspace, size_t ws_bytes,
+                                void* stream) {
     g_msg[0] = 0;
     dfa_status st = check_whole(dt, B, H, H_kv, S, D, n_chunks, scale, sched, workspace, ws_bytes, false);
-    if (st || (int64_t)B * S == 0) return st;
+    if (st || (window && (st = check_window(causal, window))) || (int64_t)B * S == 0) return st;
     if ((st = check_ptrs({q, k, v, O, lse}))) return st;
-    const AttnProblem p = whole_problem(B, H, H_kv, S, D, causal, scale);
+    const AttnProblem p = whole_problem(B, H, H_kv, S, D, causal, scale, n_chunks, window);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (dt == DFA_F32) {
         st = simt_fwd(p, dt, q, k, v, O, true, lse, s);
@@ -299,15 +310,33 @@ extern "C" dfa_status dfa_attn_fwd(const void* q, const void* k, const void* v, 
     return st;
 }
 
-extern "C" dfa_status dfa_attn_bwd(const void* q, const void* k, const void* v, const void* O, const float* lse,
-                                   const void* dO, dfa_dtype dt, int B, int H, int H_kv, int S, int D,
-                                   int n_chunks, int causal, float scale, dfa_sched sched, void* dQ, void* dK,
-                                   void* dV, void* workspace, size_t ws_bytes, void* stream) {
+extern "C" dfa_status dfa_attn_fwd(const void* q, const void* k, const void* v, dfa_dtype dt, int B, int H,
+                                   int H_kv, int S, int D, int n_chunks, int causal, float scale,
+                                   dfa_sched sched, void* O, float* lse, void* workspace, size_t ws_bytes,
+                                   void* stream) {
+    return attn_fwd_impl(q, k, v, dt, B, H, H_kv, S, D, n_chunks, causal, 0, scale, sched, O, lse, workspace,
+                         ws_bytes, stream);
+}
+
+extern "C" dfa_status dfa_attn_fwd_local(const void* q, const void* k, const void* v, dfa_dtype dt, int B,
+                                         int H, int H_kv, int S, int D, int n_chunks, int window, float scale,
+                                         dfa_sched sched, void* O, float* lse, void* workspace,
+                                         size_t ws_bytes, void* stream) {
+    g_msg[0] = 0;
+    if (window < 1) return fail(DFA_ERR_INVALID_ARG, "window must be at least one chunk (got %d)", window);
+    return attn_fwd_impl(q, k, v, dt, B, H, H_kv, S, D, n_chunks, 1, window, scale, sched, O, lse, workspace,
+                         ws_bytes, stream);
+}
+
+static dfa_status attn_bwd_impl(const void* q, const void* k, const void* v, const void* O, const float* lse,
+                                const void* dO, dfa_dtype dt, int B, int H, int H_kv, int S, int D,
+                                int n_chunks, int causal, int window, float scale, dfa_sched sched, void* dQ,
+                                void* dK, void* dV, void* workspace, size_t ws_bytes, void* stream) {
     g_msg[0] = 0;
     dfa_status st = check_whole(dt, B, H, H_kv, S, D, n_chunks, scale, sched, workspace, ws_bytes, true);
-    if (st || (int64_t)B * S == 0) return st;
+    if (st || (window && (st = check_window(causal, window))) || (int64_t)B * S == 0) return st;
     if ((st = check_ptrs({q, k, v, O, lse, dO, dQ, dK, dV}))) return st;
-    const AttnProblem p = whole_problem(B, H, H_kv, S, D, causal, scale);
+    const AttnProblem p = whole_problem(B, H, H_kv, S, D, causal, scale, n_chunks, window);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const Layout L = layout(B, H, H_kv, S, D, true);
     char* ws = static_cast<char*>(workspace);
@@ -337,6 +366,25 @@ extern "C" dfa_status dfa_attn_bwd(const void* q, const void* k, const void* v, 
     st = launch_convert(dt, B, H, S, D, scale, dq_acc, dQ, false, s);
     if (st == DFA_OK) count_launch(DFA_KERNEL_CONVERT);
     return st;
+}
+
+extern "C" dfa_status dfa_attn_bwd(const void* q, const void* k, const void* v, const void* O, const float* lse,
+                                   const void* dO, dfa_dtype dt, int B, int H, int H_kv, int S, int D,
+                                   int n_chunks, int causal, float scale, dfa_sched sched, void* dQ, void* dK,
+                                   void* dV, void* workspace, size_t ws_bytes, void* stream) {
+    return attn_bwd_impl(q, k, v, O, lse, dO, dt, B, H, H_kv, S, D, n_chunks, causal, 0, scale, sched, dQ, dK,
+                         dV, workspace, ws_bytes, stream);
+}
+
+extern "C" dfa_status dfa_attn_bwd_local(const void* q, const void* k, const void* v, const void* O,
+                                         const float* lse, const void* dO, dfa_dtype dt, int B, int H, int H_kv,
+                                         int S, int D, int n_chunks, int window, float scale, dfa_sched sched,
+                                         void* dQ, void* dK, void* dV, void* workspace, size_t ws_bytes,
+                                         void* stream) {
+    g_msg[0] = 0;
+    if (window < 1) return fail(DFA_ERR_INVALID_ARG, "window must be at least one chunk (got %d)", window);
+    return attn_bwd_impl(q, k, v, O, lse, dO, dt, B, H, H_kv, S, D, n_chunks, 1, window, scale, sched, dQ, dK,
+                         dV, workspace, ws_bytes, stream);
 }
 
 // ---------------------------------------------------------------- chunk-pair backward

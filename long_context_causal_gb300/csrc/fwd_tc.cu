@@ -60,6 +60,8 @@ struct FwdArgs {
     int B, H, Hkv, Lq, Lkv;
     int64_t q_offset, kv_offset;
     int causal;
+    int64_t win_c;         // local window: chunk length (tokens) ...
+    int win_w;             // ... and chunks per window (0: no window)
     float scale_log2;      // scale * log2(e)
     void* O;               // dense [B, Lq, H, D], bf16 or fp32
     float* lse;            // [B, H, Lq]
@@ -72,10 +74,15 @@ struct FwdArgs {
 };
 
 struct Item {
-    int b, h, g, q0, n_kv;
+    int b, h, g, q0, j0, n_kv;   // key/value tiles [j0, n_kv) can be visible to the block
 };
 
-__device__ __forceinline__ Item decode(const FwdArgs& a, int it) {
+// First key position a query at position qp may see under the local window.
+__device__ __forceinline__ int64_t window_lo(const FwdArgs& a, int64_t qp) {
+    return (qp / a.win_c - (a.win_w - 1)) * a.win_c;
+}
+
+__device__ __forceinline__ Item decode(const FwdArgs& a, int it, bool win) {
     Item x;
     const int row = it / a.n_units, unit = it % a.n_units;
     x.b = row / a.H;
@@ -91,15 +98,20 @@ __device__ __forceinline__ Item decode(const FwdArgs& a, int it) {
         const int64_t tiles = (visible + BN - 1) / BN;
         x.n_kv = visible <= 0 ? 0 : (int)(tiles < total ? tiles : total);
     }
+    x.j0 = 0;
+    if (win) {   // the block's first row has the lowest window start
+        const int64_t lo = window_lo(a, a.q_offset + x.q0) - a.kv_offset;
+        x.j0 = lo <= 0 ? 0 : (int)(lo / BN < x.n_kv ? lo / BN : x.n_kv);
+    }
     return x;
 }
 
-// Row max of this thread's 128 scores in TMEM (columns >= lim masked when MASK).
+// Row max of this thread's 128 scores in TMEM (columns outside [lo, lim) masked when MASK).
 // Four independent accumulators keep the dependent chain short; the chunk
 // loop stays rolled to keep the kernel's code small (several roles run
 // different code at once and share the instruction cache).
 template <bool MASK>
-__device__ __forceinline__ float row_max(uint32_t tS, int lim) {
+__device__ __forceinline__ float row_max(uint32_t tS, int lo, int lim) {
     float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
@@ -108,7 +120,7 @@ __device__ __forceinline__ float row_max(uint32_t tS, int lim) {
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
             const float x = __uint_as_float(u[e]);
-            m[e & 3] = fmaxf(m[e & 3], (!MASK || c * 32 + e < lim) ? x : -INFINITY);
+            m[e & 3] = fmaxf(m[e & 3], (!MASK || (c * 32 + e >= lo && c * 32 + e < lim)) ? x : -INFINITY);
         }
     }
     return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
@@ -118,7 +130,7 @@ __device__ __forceinline__ float row_max(uint32_t tS, int lim) {
 // first 64 TMEM columns of S (behind the columns still to be read).  Returns
 // the row sum of the fp32 P values.
 template <bool MASK>
-__device__ __forceinline__ float row_exp(uint32_t tS, int lim, float c2, float m) {
+__device__ __forceinline__ float row_exp(uint32_t tS, int lo, int lim, float c2, float m) {
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
@@ -131,8 +143,8 @@ __device__ __forceinline__ float row_exp(uint32_t tS, int lim, float c2, float m
             float p0 = ex2(fmaf(__uint_as_float(u[2 * e]), c2, -m));
             float p1 = ex2(fmaf(__uint_as_float(u[2 * e + 1]), c2, -m));
             if (MASK) {
-                p0 = c0 < lim ? p0 : 0.f;
-                p1 = c0 + 1 < lim ? p1 : 0.f;
+                p0 = c0 >= lo && c0 < lim ? p0 : 0.f;
+                p1 = c0 + 1 >= lo && c0 + 1 < lim ? p1 : 0.f;
             }
             acc[e & 3] += p0 + p1;
             pk[e] = pack_bf16(p0, p1);
@@ -142,7 +154,8 @@ __device__ __forceinline__ float row_exp(uint32_t tS, int lim, float c2, float m
     return (acc[0] + acc[1]) + (acc[2] + acc[3]);
 }
 
-template <int D, bool OUT_F32>
+// WIN: local window (its range and mask code is compiled only into this variant).
+template <int D, bool OUT_F32, bool WIN>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
@@ -207,8 +220,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         uint32_t ld = 0, qi = 0, qi_issued = 0;
         bool ok = true;
         for (int it = it_begin; it < it_end && ok; ++it) {
-            const Item x = decode(a, a.wl_items ? a.wl_items[it] : it);
-            if (x.n_kv == 0) continue;
+            const Item x = decode(a, a.wl_items ? a.wl_items[it] : it, WIN);
+            if (x.n_kv <= x.j0) continue;
             ok = __all_sync(0xffffffffu, mbar_wait_acc(q_empty, (qi & 1) ^ 1, abort_flag, a.err, nullptr));
             if (!ok) break;
             ++qi_issued;
@@ -220,7 +233,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                                     x.q0 + w * BM, x.b);
             }
             __syncwarp();
-            for (int j = 0; j < x.n_kv && ok; ++j) {
+            for (int j = x.j0; j < x.n_kv && ok; ++j) {
                 for (int which = 0; which < 2; ++which, ++ld) {
                     const int slot = ld % C::kSlots;
                     ok = __all_sync(0xffffffffu, mbar_wait_acc(&kv_empty[slot], ((ld / C::kSlots) & 1) ^ 1,
@@ -291,8 +304,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         };
         auto commit = [&](uint64_t* bar) { mma_commit(bar); };
         for (int it = it_begin; it < it_end && ok; ++it) {
-            const Item x = decode(a, a.wl_items ? a.wl_items[it] : it);
-            if (x.n_kv == 0) continue;
+            const Item x = decode(a, a.wl_items ? a.wl_items[it] : it, WIN);
+            if (x.n_kv <= x.j0) continue;
             if (!wait(q_full, qi & 1)) break;
             uint32_t slotK = cons % C::kSlots;
             if (!wait(&kv_full[slotK], (cons / C::kSlots) & 1)) break;
@@ -302,12 +315,12 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             commit(&s_full[1]);
             commit(&kv_empty[slotK]);
             ++cons;
-            for (int j = 0; j < x.n_kv && ok; ++j, ++t) {
+            for (int j = x.j0; j < x.n_kv && ok; ++j, ++t) {
                 const bool more = j + 1 < x.n_kv;
                 const uint32_t slotV = cons % C::kSlots;
                 if (!wait(&kv_full[slotV], (cons / C::kSlots) & 1)) break;
                 if (!wait(&p_full[0], t & 1)) break;
-                issue_PV(0, slotV, j > 0);
+                issue_PV(0, slotV, j > x.j0);
                 if (!more) commit(&o_full[0]);
                 uint32_t slotK1 = (cons + 1) % C::kSlots;
                 if (more) {
@@ -316,7 +329,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     commit(&s_full[0]);
                 }
                 if (!wait(&p_full[1], t & 1)) break;
-                issue_PV(1, slotV, j > 0);
+                issue_PV(1, slotV, j > x.j0);
                 commit(&kv_empty[slotV]);
                 if (!more) commit(&o_full[1]);
                 if (more) {
@@ -346,11 +359,15 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         uint32_t t = 0, qi = 0;
         bool ok = true;
         for (int it = it_begin; it < it_end && ok; ++it) {
-            const Item x = decode(a, a.wl_items ? a.wl_items[it] : it);
+            const Item x = decode(a, a.wl_items ? a.wl_items[it] : it, WIN);
             const int row = x.q0 + w * BM + r;                 // row within the query chunk
             const int64_t qpos = a.q_offset + row;
             float m_run = -INFINITY, l = 0.f;
-            for (int j = 0; j < x.n_kv; ++j, ++t) {
+            // local window: this row's first visible key (relative to the chunk's keys),
+            // and the highest such start among the tile's rows (decides the mask path)
+            const int64_t lo_row = WIN ? window_lo(a, qpos) - a.kv_offset : INT64_MIN;
+            const int64_t lo_tile = WIN ? window_lo(a, a.q_offset + x.q0 + w * BM + BM - 1) - a.kv_offset : INT64_MIN;
+            for (int j = x.j0; j < x.n_kv; ++j, ++t) {
                 ok = __all_sync(0xffffffffu, mbar_wait_acc(&s_full[w], t & 1, abort_flag, a.err, nullptr));
                 if (!ok) break;
                 tc_fence_after();
@@ -358,10 +375,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 const int kv0 = j * BN;
                 const bool edge = kv0 + BN > a.Lkv;
                 const bool diag = a.causal && (a.kv_offset + kv0 + BN - 1 > a.q_offset + x.q0 + w * BM);
-                const bool masked = edge || diag;
-                // Column c of this tile is visible iff c < lim (both conditions are prefix limits).
-                int lim = BN;
+                const bool masked = edge || diag || (WIN && kv0 < lo_tile);
+                // Column c of this tile is visible iff lo <= c < lim.
+                int lo = 0, lim = BN;
                 if (masked) {
+                    if (WIN && lo_row > kv0) lo = lo_row - kv0 > BN ? BN : (int)(lo_row - kv0);
                     int64_t v = (int64_t)a.Lkv - kv0;
                     if (a.causal) {
                         const int64_t vc = qpos - a.kv_offset - kv0 + 1;
@@ -369,7 +387,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     }
                     lim = v < 0 ? 0 : (v > BN ? BN : (int)v);
                 }
-                const float mx = masked ? row_max<true>(tS, lim) : row_max<false>(tS, lim);
+                const float mx = masked ? row_max<true>(tS, lo, lim) : row_max<false>(tS, lo, lim);
                 const float mx2 = mx * c2;
                 // Lazy rescale: move this row's reference max only when the tile
                 // max exceeds it by more than 2^8.  The decision is per row, but
@@ -385,7 +403,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     }
                     m_run = mx2;
                 }
-                if (j > 0 && __any_sync(0xffffffffu, resc)) {
+                if (j > x.j0 && __any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t u[32];
@@ -397,7 +415,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 }
                 const float m_use = m_run == -INFINITY ? 0.f : m_run;
                 // Pass 2: P = exp2(s * c2 - m), row sum, bf16 P written over S.
-                l += masked ? row_exp<true>(tS, lim, c2, m_use) : row_exp<false>(tS, lim, c2, m_use);
+                l += masked ? row_exp<true>(tS, lo, lim, c2, m_use) : row_exp<false>(tS, lo, lim, c2, m_use);
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(&p_full[w]);
@@ -407,7 +425,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             const bool valid_row = row < a.Lq;
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const int64_t orow = (((int64_t)x.b * a.Lq + row) * a.H + x.h) * D;
-            if (x.n_kv > 0) {
+            if (x.n_kv > x.j0) {
                 ok = __all_sync(0xffffffffu, mbar_wait_acc(&o_full[w], qi & 1, abort_flag, a.err, nullptr));
                 if (!ok) break;
                 tc_fence_after();
@@ -509,6 +527,7 @@ static dfa_status launch(const AttnProblem& p, const void* q, const void* k, con
     FwdArgs a{};
     a.B = p.B; a.H = p.H; a.Hkv = p.Hkv; a.Lq = p.Lq; a.Lkv = p.Lkv;
     a.q_offset = p.q_offset; a.kv_offset = p.kv_offset; a.causal = p.causal;
+    a.win_c = p.win_c; a.win_w = p.causal ? p.win_w : 0;
     a.scale_log2 = p.scale * kLog2e;
     a.O = O; a.lse = lse;
     a.n_units = (p.Lq + kBlockRows - 1) / kBlockRows;
@@ -524,7 +543,7 @@ static dfa_status launch(const AttnProblem& p, const void* q, const void* k, con
         a.wl_items = nullptr;
         grid = p.B * p.H * a.n_units;
     }
-    auto kern = fwd_tc_kernel<D, OUT_F32>;
+    auto kern = a.win_w > 0 ? fwd_tc_kernel<D, OUT_F32, true> : fwd_tc_kernel<D, OUT_F32, false>;
     const int smem = Cfg<D>::kSmem;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return fail(DFA_ERR_CUDA, "fwd_tc: shared memory attribute");

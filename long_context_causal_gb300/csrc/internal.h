@@ -19,6 +19,9 @@ struct AttnProblem {
     int causal;
     float scale;
     int acc_out;                  // backward outputs are fp32 accumulators (+=)
+    int64_t win_c;                // local window (causal only): chunk length in tokens ...
+    int win_w;                    // ... and chunks per window; key kp is visible from query qp iff
+                                  // kp <= qp and kp / win_c >= qp / win_c - (win_w - 1).  0: none
 };
 
 // Device error flag (set by bounded waits that gave up).  Returns the device

@@ -37,6 +37,10 @@ template <> __device__ __forceinline__ void st<float>(float* p, float x) { *p = 
 template <> __device__ __forceinline__ void st<__nv_bfloat16>(__nv_bfloat16* p, float x) {
     *p = __float2bfloat16_rn(x);
 }
+// Key position kp lies outside the local window of query position qp.
+__device__ __forceinline__ bool out_of_window(const AttnProblem& p, int64_t qp, int64_t kp) {
+    return p.win_w > 0 && p.causal && kp / p.win_c < qp / p.win_c - (p.win_w - 1);
+}
 // Store, or add to the value already there (each output element has one writer).
 template <typename T> __device__ __forceinline__ void put(T* p, float x, bool acc) { st(p, acc ? ld(p) + x : x); }
 
@@ -110,8 +114,10 @@ simt_fwd_kernel(AttnProblem p, const T* __restrict__ q, const T* __restrict__ k,
                 sb = fmaf(Qs[row][d], Ks[lane + 32][d], sb);
             }
             const int ja = kt + lane, jb = kt + lane + 32;
-            if (ja >= p.Lkv || (p.causal && p.kv_offset + ja > qpos)) sa = -INFINITY;
-            if (jb >= p.Lkv || (p.causal && p.kv_offset + jb > qpos)) sb = -INFINITY;
+            if (ja >= p.Lkv || (p.causal && p.kv_offset + ja > qpos) || out_of_window(p, qpos, p.kv_offset + ja))
+                sa = -INFINITY;
+            if (jb >= p.Lkv || (p.causal && p.kv_offset + jb > qpos) || out_of_window(p, qpos, p.kv_offset + jb))
+                sb = -INFINITY;
             const float mn = fmaxf(m[r], warp_max(fmaxf(sa, sb)));
             if (mn == -INFINITY) continue;          // nothing visible yet in this row
             const float alpha = exp2f(m[r] - mn);   // 0 when m was -inf
@@ -202,8 +208,10 @@ simt_bwd_dq_kernel(AttnProblem p, const T* __restrict__ q, const T* __restrict__
                 pb_ = fmaf(dOs[row][d], Vs[lane + 32][d], pb_);
             }
             const int ja = kt + lane, jb = kt + lane + 32;
-            const bool va = ja < p.Lkv && !(p.causal && p.kv_offset + ja > qpos);
-            const bool vb_ = jb < p.Lkv && !(p.causal && p.kv_offset + jb > qpos);
+            const bool va = ja < p.Lkv && !(p.causal && p.kv_offset + ja > qpos) &&
+                            !out_of_window(p, qpos, p.kv_offset + ja);
+            const bool vb_ = jb < p.Lkv && !(p.causal && p.kv_offset + jb > qpos) &&
+                             !out_of_window(p, qpos, p.kv_offset + jb);
             const float Pa = va ? exp2f(sa - lse2[r]) : 0.f;
             const float Pb = vb_ ? exp2f(sb - lse2[r]) : 0.f;
             const float dsa = Pa * (pa_ - dl[r]), dsb = Pb * (pb_ - dl[r]);
@@ -289,7 +297,8 @@ simt_bwd_dkv_kernel(AttnProblem p, const T* __restrict__ q, const T* __restrict_
                         dp = fmaf(dOs[ir][d], Vs[jr][d], dp);
                     }
                     const bool vis = (j0 + jr < p.Lkv) && (qt + ir < p.Lq) && lse2s[ir] != -INFINITY &&
-                                     !(p.causal && kpos > p.q_offset + qt + ir);
+                                     !(p.causal && kpos > p.q_offset + qt + ir) &&
+                                     !out_of_window(p, p.q_offset + qt + ir, kpos);
                     Pv[half] = vis ? exp2f(s * c2 - lse2s[ir]) : 0.f;
                     dS[half] = Pv[half] * (dp - dls[ir]);
                 }

@@ -52,6 +52,9 @@ def _load() -> ctypes.CDLL:
         "dfa_chunk_attn_bwd": (i32, [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i64, i64, i32, f32,
                                      vp, vp, vp, vp, sz, vp]),
         "dfa_chunk_bwd_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
+        "dfa_attn_fwd_local": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, f32, i32, vp, vp, vp, sz, vp]),
+        "dfa_attn_bwd_local": (i32, [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, f32, i32,
+                                     vp, vp, vp, vp, sz, vp]),
         "dfa_attn_fwd_noalloc": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, f32, i32, vp, vp, vp]),
         "dfa_check_errors": (i32, [vp]),
         "dfa_last_error": (ctypes.c_char_p, []),
@@ -239,6 +242,42 @@ def dfa_attn_bwd(q, k, v, O, lse, dO, n_chunks: int = 1, causal: bool = True,
     _check(_lib.dfa_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(O), _ptr(lse), _ptr(dO), _dtype(q),
                              B, H, Hkv, S, D, int(n_chunks), int(bool(causal)), scale, _SCHED[sched],
                              _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(ws), ws.numel(), _stream(stream)))
+    return dQ, dK, dV
+
+
+def dfa_attn_fwd_local(q, k, v, n_chunks: int, window: int, scale: float | None = None, sched="balanced",
+                       O=None, lse=None, workspace_buf=None, stream=None):
+    """Causal forward restricted to a local window of `window` chunks (S / n_chunks
+    tokens each): returns (O, lse) like dfa_attn_fwd."""
+    B, S, H, D = q.shape
+    Hkv = k.shape[2]
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _dense(t, n)
+    scale = D ** -0.5 if scale is None else float(scale)
+    O = torch.empty_like(q) if O is None else O
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device) if lse is None else lse
+    ws = workspace(B, H, Hkv, S, D, n_chunks, False, q.device) if workspace_buf is None else workspace_buf
+    _check(_lib.dfa_attn_fwd_local(_ptr(q), _ptr(k), _ptr(v), _dtype(q), B, H, Hkv, S, D, int(n_chunks),
+                                   int(window), scale, _SCHED[sched], _ptr(O), _ptr(lse), _ptr(ws), ws.numel(),
+                                   _stream(stream)))
+    return O, lse
+
+
+def dfa_attn_bwd_local(q, k, v, O, lse, dO, n_chunks: int, window: int, scale: float | None = None,
+                       sched="balanced", dQ=None, dK=None, dV=None, workspace_buf=None, stream=None):
+    """Backward of dfa_attn_fwd_local from the saved (O, lse): returns (dQ, dK, dV)."""
+    B, S, H, D = q.shape
+    Hkv = k.shape[2]
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (O, "O"), (lse, "lse"), (dO, "dO")):
+        _dense(t, n)
+    scale = D ** -0.5 if scale is None else float(scale)
+    dQ = torch.empty_like(q) if dQ is None else dQ
+    dK = torch.empty_like(k) if dK is None else dK
+    dV = torch.empty_like(v) if dV is None else dV
+    ws = workspace(B, H, Hkv, S, D, n_chunks, True, q.device) if workspace_buf is None else workspace_buf
+    _check(_lib.dfa_attn_bwd_local(_ptr(q), _ptr(k), _ptr(v), _ptr(O), _ptr(lse), _ptr(dO), _dtype(q),
+                                   B, H, Hkv, S, D, int(n_chunks), int(window), scale, _SCHED[sched],
+                                   _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(ws), ws.numel(), _stream(stream)))
     return dQ, dK, dV
 
 

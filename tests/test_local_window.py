@@ -1,0 +1,79 @@
+"""Local sliding window (DISTFLASHATTN App. F) through the C ABI against the
+fp64 oracle: a query sees its own chunk and the window - 1 chunks before it.
+
+Cases cover chunk lengths that are multiples of the 256-row forward block, of
+the 128-row tile only (a block straddles two windows), and of neither (the
+window edge cuts through tiles), head dims 128 and 64, GQA, and fp32 on the
+CUDA-core kernels.  Tolerances as in the other parity tests.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from long_context_causal_gb300 import dfa
+from long_context_causal_gb300.inputs import make
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def np64(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def check(O, lse, grads, Or, lr, refs, dtype, what):
+    if dtype == torch.float32:
+        assert np.max(np.abs(np64(O) - Or)) <= 1e-4, f"{what}: O"
+        assert np.max(np.abs(np64(lse) - lr)) <= 1e-5, f"{what}: lse"
+    else:
+        assert np.max(np.abs(np64(O) - Or)) <= 2e-2, f"{what}: O"
+        assert np.max(np.abs(np64(lse) - lr)) <= 1e-3, f"{what}: lse"
+    for name, g, r in zip(("dQ", "dK", "dV"), grads, refs):
+        err = np.max(np.abs(np64(g) - r))
+        if dtype == torch.float32:
+            assert err <= 1e-3, f"{what}: {name} abs err {err}"
+        else:
+            rel = err / max(np.max(np.abs(r)), 1e-2)
+            assert rel <= 3e-2, f"{what}: {name} rel err {rel}"
+
+
+# (B, H, Hkv, S, D, dtype, n_chunks, window, note)
+CASES = [
+    (1, 4, 2, 1024, 128, torch.bfloat16, 4, 2, "C=256, two chunks"),
+    (1, 2, 1, 1536, 128, torch.bfloat16, 4, 1, "C=384: a 256-row block straddles windows"),
+    (1, 2, 2, 1280, 128, torch.bfloat16, 4, 2, "C=320: the window edge cuts through tiles"),
+    (2, 2, 1, 1024, 128, torch.bfloat16, 8, 3, "C=128, three chunks, batch 2"),
+    (1, 2, 2, 768, 64, torch.bfloat16, 3, 2, "D=64"),
+    (1, 2, 1, 300, 64, torch.float32, 3, 2, "fp32 on CUDA cores"),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[-1] for c in CASES])
+def test_local_window_matches_oracle(case):
+    B, H, Hkv, S, D, dtype, P, w, what = case
+    q, k, v, do = make(B, H, Hkv, S, D, dtype, device=DEV, seed=21)
+    O, lse = dfa.dfa_attn_fwd_local(q, k, v, n_chunks=P, window=w)
+    grads = dfa.dfa_attn_bwd_local(q, k, v, O, lse, do, n_chunks=P, window=w)
+    dfa.dfa_check_errors()
+    C = S // P
+    Or, lr = oracle.attn_fwd_local(np64(q), np64(k), np64(v), chunk=C, window=w)
+    refs = oracle.attn_bwd_local(np64(q), np64(k), np64(v), np64(do), chunk=C, window=w)
+    check(O, lse, grads, Or, lr, refs, dtype, what)
+
+
+def test_window_covering_all_chunks_gives_the_causal_bits():
+    q, k, v, do = make(1, 2, 2, 1024, 128, torch.bfloat16, device=DEV, seed=22)
+    O1, l1 = dfa.dfa_attn_fwd_local(q, k, v, n_chunks=4, window=4)
+    O2, l2 = dfa.dfa_attn_fwd(q, k, v, n_chunks=4)
+    assert torch.equal(O1, O2) and torch.equal(l1, l2)
+    g1 = dfa.dfa_attn_bwd_local(q, k, v, O1, l1, do, n_chunks=4, window=4)
+    g2 = dfa.dfa_attn_bwd(q, k, v, O2, l2, do, n_chunks=4)
+    for a, b in zip(g1, g2):
+        torch.testing.assert_close(a, b, rtol=0, atol=2e-3)   # dQ adds in a different order (atomics)
+
+
+def test_bad_window_is_rejected():
+    q, k, v, do = make(1, 2, 2, 256, 128, torch.bfloat16, device=DEV, seed=23)
+    with pytest.raises(dfa.DfaError):
+        dfa.dfa_attn_fwd_local(q, k, v, n_chunks=2, window=0)
