@@ -44,6 +44,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-chunk-step", action="store_true", help="skip the per-worker chunk-step timing")
+    ap.add_argument("--window", type=int, default=2, help="chunks per local window for the extra local-window timing (0: skip)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target oracle sample time")
     return ap.parse_args()
 
@@ -272,6 +273,55 @@ def chunk_step_timing(w, q, k, v, O, lse, do, stream, dfa, reps=5):
     return out
 
 
+def local_window_pairs(S, C, window):
+    """Visible (query, key) pairs per head of causal attention restricted to a
+    local window of `window` chunks of C tokens."""
+    import numpy as np
+    qp = np.arange(S, dtype=np.int64)
+    lo = np.maximum(0, (qp // C - (window - 1)) * C)
+    return int(np.sum(qp - lo + 1))
+
+
+def local_window_timing(w, window, q, k, v, do, stream, dfa, reps=3):
+    """Forward + backward with the pages' local sliding window (App. F) on the
+    same workload; FLOPs counted on the visible pairs only.  Reported beside
+    the headline, not part of it."""
+    import torch
+    if w.n_chunks < 2 or window >= w.n_chunks:
+        return None
+    C = w.S // w.n_chunks
+    O = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=q.device)
+    dQ, dK, dV = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    wsf = dfa.workspace(w.B, w.H, w.H_kv, w.S, w.D, w.n_chunks, False, q.device)
+    wsb = dfa.workspace(w.B, w.H, w.H_kv, w.S, w.D, w.n_chunks, True, q.device)
+
+    def fwd():
+        dfa.dfa_attn_fwd_local(q, k, v, n_chunks=w.n_chunks, window=window, scale=w.scale, O=O, lse=lse,
+                               workspace_buf=wsf, stream=stream)
+
+    def bwd():
+        dfa.dfa_attn_bwd_local(q, k, v, O, lse, do, n_chunks=w.n_chunks, window=window, scale=w.scale,
+                               dQ=dQ, dK=dK, dV=dV, workspace_buf=wsb, stream=stream)
+
+    pairs = w.B * w.H * local_window_pairs(w.S, C, window)
+    out = {"window": window, "chunk": C}
+    for tag, fn, per_pair in (("fwd", fwd, 4), ("bwd", bwd, 10)):
+        fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(q.device)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(q.device)
+        ms = a.elapsed_time(b) / reps
+        out[f"{tag}_ms"] = ms
+        out[f"{tag}_tflops"] = pairs * w.D * per_pair / (ms * 1e-3) / 1e12
+    dfa.dfa_check_errors(stream)
+    return out
+
+
 # ---------------------------------------------------------------- GPU arm
 def main():
     args = parse()
@@ -391,6 +441,7 @@ def main():
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": n_e2e}
 
     chunk = None if args.no_chunk_step else chunk_step_timing(w, q, k, v, O, lse, do, stream, dfa)
+    local = None if args.window <= 0 else local_window_timing(w, args.window, q, k, v, do, stream, dfa)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -419,6 +470,7 @@ def main():
                          "frac": fwd_tflops / peak_tc},
         "cpu_baseline": cpu,
         "chunk_step": chunk,
+        "local_window": local,
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clk,
