@@ -62,8 +62,8 @@ typedef enum { DFA_F32 = 0, DFA_BF16 = 1 } dfa_dtype;
  *   so every worker gets the same amount of work to within one pair. */
 typedef enum { DFA_SCHED_BALANCED = 0, DFA_SCHED_UNBALANCED = 1 } dfa_sched;
 
-/* One chunk step (DISTFLASHATTN App. D: "update the attention state, return
- * the output and its log-sum-exp"): a query chunk of Lq rows at global
+/* One chunk step (DISTFLASHATTN App. D: a worker's step advances its attention
+ * state and hands back the output with its log-sum-exp): a query chunk of Lq rows at global
  * position q_offset against a key/value chunk of Lkv rows at kv_offset.
  *   q:        [B, Lq, H, D] with element strides q_strides = {batch, seq, head}
  *   k, v:     [B, Lkv, H_kv, D] with element strides kv_strides (shared by k, v)
