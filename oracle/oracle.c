@@ -14,8 +14,8 @@
  *   - §3.2: a query only attends to its causal prefix; helpers return a partial
  *     output plus softmax statistics which the owner rescales and merges (the
  *     online-normalizer rule of "Online normalizer calculation for softmax");
- *   - §1/§3.3: the backward reuses the saved output and log-sum-exp, "without
- *     numerical differences" from recomputation, i.e. the backward is the exact
+ *   - §1/§3.3: the backward reuses the saved output and log-sum-exp, and this
+ *     rematerialisation changes no numbers, i.e. the backward is the exact
  *     gradient of the same attention.
  *
  * The pages print no formulas; the readings taken here are the textbook ones:
