@@ -45,6 +45,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-chunk-step", action="store_true", help="skip the per-worker chunk-step timing")
     ap.add_argument("--window", type=int, default=2, help="chunks per local window for the extra local-window timing (0: skip)")
+    ap.add_argument("--no-split-kv", action="store_true", help="skip the small-problem split-kv forward timing")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target oracle sample time")
     return ap.parse_args()
 
@@ -322,6 +323,45 @@ def local_window_timing(w, window, q, k, v, do, stream, dfa, reps=3):
     return out
 
 
+SPLIT_KV_SHAPES = [(1, 1, 1, 32768, 128), (1, 4, 4, 8192, 128)]
+
+
+def split_kv_timing(device, stream, dfa, reps=10):
+    """Causal forward of problems with fewer 256-row query blocks than SMs, with the
+    plain balanced list and with split-kv helper items (pieces of each block's
+    key range computed by other CTAs, then merged).  Inputs of these sizes stay
+    in L2; the forward is compute-bound either way.  Reported beside the headline."""
+    import torch
+    from long_context_causal_gb300.inputs import make
+    out = []
+    for B, H, Hkv, S, D in SPLIT_KV_SHAPES:
+        q, k, v, _ = make(B, H, Hkv, S, D, torch.bfloat16, seed=3, device=device)
+        O = torch.empty_like(q)
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=device)
+        ws = dfa.workspace(B, H, Hkv, S, D, 1, False, device)
+        flops = B * H * S * (S + 1) // 2 * D * 4
+        row = {"B": B, "H": H, "H_kv": Hkv, "S": S, "D": D}
+        for sched in ("balanced", "split_kv"):
+            def fwd():
+                dfa.dfa_attn_fwd(q, k, v, sched=sched, O=O, lse=lse, workspace_buf=ws, stream=stream)
+            for _ in range(3):
+                fwd()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(device)
+            a.record(stream)
+            for _ in range(reps):
+                fwd()
+            b.record(stream)
+            torch.cuda.synchronize(device)
+            ms = a.elapsed_time(b) / reps
+            row[f"{sched}_fwd_ms"] = ms
+            row[f"{sched}_fwd_tflops"] = flops / (ms * 1e-3) / 1e12
+        row["speedup"] = row["balanced_fwd_ms"] / row["split_kv_fwd_ms"]
+        out.append(row)
+    dfa.dfa_check_errors(stream)
+    return out
+
+
 # ---------------------------------------------------------------- GPU arm
 def main():
     args = parse()
@@ -442,6 +482,7 @@ def main():
 
     chunk = None if args.no_chunk_step else chunk_step_timing(w, q, k, v, O, lse, do, stream, dfa)
     local = None if args.window <= 0 else local_window_timing(w, args.window, q, k, v, do, stream, dfa)
+    split = None if args.no_split_kv else split_kv_timing(q.device, stream, dfa)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -471,6 +512,7 @@ def main():
         "cpu_baseline": cpu,
         "chunk_step": chunk,
         "local_window": local,
+        "split_kv": split,
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clk,

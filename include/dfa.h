@@ -59,8 +59,17 @@ typedef enum { DFA_F32 = 0, DFA_BF16 = 1 } dfa_dtype;
  * BALANCED: the token-level balanced schedule -- a worker that takes an
  *   early (cheap) query tile also takes its mirror image at the end of the
  *   sequence, and these equal-cost pairs are dealt to the workers in turn,
- *   so every worker gets the same amount of work to within one pair. */
-typedef enum { DFA_SCHED_BALANCED = 0, DFA_SCHED_UNBALANCED = 1 } dfa_sched;
+ *   so every worker gets the same amount of work to within one pair.
+ * SPLIT_KV: BALANCED plus helper items (§3.2: idle workers compute part of a
+ *   busy worker's attention and hand back a partial output with its
+ *   log-sum-exp, which the owner merges).  When a bf16 whole-sequence forward
+ *   has fewer 256-row query blocks than the GPU has SMs, every block's
+ *   key/value range is cut into pieces of dfa_split_piece_tiles() 128-key
+ *   tiles; each piece is an item of its own whose fp32 partial (O, lse) goes
+ *   to the workspace, and a merge kernel combines each row's pieces with the
+ *   rescale-and-merge rule.  Larger problems, the local window, fp32 I/O, the
+ *   no-alloc forward and every backward treat it as BALANCED. */
+typedef enum { DFA_SCHED_BALANCED = 0, DFA_SCHED_UNBALANCED = 1, DFA_SCHED_SPLIT_KV = 2 } dfa_sched;
 
 /* One chunk step (DISTFLASHATTN App. D: a worker's step advances its attention
  * state and hands back the output with its log-sum-exp): a query chunk of Lq rows at global
@@ -221,6 +230,25 @@ int64_t dfa_launch_count(dfa_kernel_kind kind);
  * per-worker cost) or -1 on bad arguments. */
 int64_t dfa_build_worklist(int n_rows, int n_units, int n_workers, dfa_sched sched,
                            int32_t* offsets, int32_t* items);
+
+/* Piece length, in 128-key tiles, that SPLIT_KV uses for a whole-sequence
+ * forward of B*H rows of S tokens on a GPU with n_sms SMs, or 0 when the
+ * problem has at least n_sms 256-row query blocks (or is too short to gain)
+ * and is not split.  Pieces hold at least 4 tiles and are sized so that the
+ * pieces number about twice n_sms. */
+int dfa_split_piece_tiles(int B, int H, int S, int causal, int n_sms);
+
+/* Work list of SPLIT_KV items.  Query block u of a row covers query tiles
+ * [2u, 2u + 2) and sees key tiles [0, hi(u)), hi(u) = min(2u + 2, kv_tiles)
+ * when causal, kv_tiles otherwise; that range is cut into pieces
+ * [s * piece_tiles, (s + 1) * piece_tiles) and only non-empty pieces become
+ * items, with value (row * n_units + u) * n_split + s, n_split =
+ * ceil(kv_tiles / piece_tiles).  Pieces are dealt longest first, each to the
+ * least-loaded worker.  offsets[n_workers + 1] as for dfa_build_worklist;
+ * items needs n_rows * n_units * n_split entries at most.  Returns the
+ * makespan in (query tile x key tile) units, or -1 on bad arguments. */
+int64_t dfa_build_split_worklist(int n_rows, int n_units, int kv_tiles, int causal, int piece_tiles,
+                                 int n_workers, int32_t* offsets, int32_t* items);
 
 /* The pages' distributed schedule at chunk-step granularity (DISTFLASHATTN
  * App. B, Figs. 5-6, and §4.5): P workers own one chunk each, a step computes

@@ -4,6 +4,8 @@
 //             (DISTFLASHATTN §3.2, paperlayer.ai summary of arXiv 2310.03294:
 //             helpers return partial outputs plus softmax statistics that the
 //             owner rescales before combining);
+//  * merge_pieces: the same rule over the split-kv pieces of a forward, fp32
+//             partials in, the output dtype out;
 //  * delta:   Delta_i = <dO_i, O_i>, the per-row term of the softmax gradient,
 //             read once from the SAVED output (§3.3: the backward reuses the
 //             forward's output instead of recomputing it);
@@ -21,6 +23,13 @@ namespace dfa {
 namespace {
 
 constexpr int kThreads = 256;
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
 __global__ void __launch_bounds__(kThreads)
 merge_kernel(int B, int H, int L, int D, const float* Oa, const float* la, const float* Ob,
@@ -186,6 +195,52 @@ dfa_status launched(const char* what) {
 
 }  // namespace
 
+// Split-kv merge (the owner's side of the pages' helper exchange, §3.2): one
+// warp per (b, i, h) row combines the row's pieces with the rescale rule
+//   lse = m + ln sum_s e^(lse_s - m),  O = sum_s e^(lse_s - lse) O_s,
+// m = max_s lse_s; pieces with lse_s = -inf weigh 0.  Every row's piece 0
+// holds key 0, so lse is finite for every row that sees a key.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+merge_pieces_kernel(int B, int H, int S, int D, int causal, int piece_tiles, int n_split, const float* O_part,
+                    const float* lse_part, T* O, float* lse) {
+    const int64_t row = (int64_t)blockIdx.x * (kThreads / 32) + threadIdx.x / 32;  // (b, i, h)
+    const int lane = threadIdx.x % 32;
+    if (row >= (int64_t)B * S * H) return;
+    const int h = row % H;
+    const int64_t bi = row / H;
+    const int i = bi % S, b = bi / S;
+    const int kv_tiles = (S + 127) / 128, u = i / 256;
+    const int hi = causal ? min(2 * u + 2, kv_tiles) : kv_tiles;
+    const int np = min((hi + piece_tiles - 1) / piece_tiles, n_split);
+    const int64_t li = ((int64_t)b * H + h) * S + i, lstride = (int64_t)B * H * S;
+    const int64_t ostride = (int64_t)B * S * H * D;
+    float m = -INFINITY;
+    for (int s = 0; s < np; ++s) m = fmaxf(m, lse_part[s * lstride + li]);
+    float sum = 0.f;
+    if (m != -INFINITY)
+        for (int s = 0; s < np; ++s) sum += expf(lse_part[s * lstride + li] - m);
+    const float inv = sum > 0.f ? 1.f / sum : 0.f;
+    for (int x = lane; x < D / 4; x += 32) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (m != -INFINITY)
+            for (int s = 0; s < np; ++s) {
+                const float w = expf(lse_part[s * lstride + li] - m) * inv;
+                const float4 o = reinterpret_cast<const float4*>(O_part + s * ostride + row * D)[x];
+                acc.x += w * o.x;
+                acc.y += w * o.y;
+                acc.z += w * o.z;
+                acc.w += w * o.w;
+            }
+        T* dst = O + row * D + 4 * x;
+        dst[0] = from_f32<T>(acc.x);
+        dst[1] = from_f32<T>(acc.y);
+        dst[2] = from_f32<T>(acc.z);
+        dst[3] = from_f32<T>(acc.w);
+    }
+    if (lane == 0) lse[li] = sum > 0.f ? m + logf(sum) : -INFINITY;
+}
+
 dfa_status launch_merge(int B, int H, int L, int D, const float* Oa, const float* la,
                         const float* Ob, const float* lb, float* O, float* l, cudaStream_t s) {
     const int64_t rows = (int64_t)B * L * H;
@@ -193,6 +248,22 @@ dfa_status launch_merge(int B, int H, int L, int D, const float* Oa, const float
     const int64_t blocks = (rows + kThreads / 32 - 1) / (kThreads / 32);
     merge_kernel<<<(unsigned)blocks, kThreads, 0, s>>>(B, H, L, D, Oa, la, Ob, lb, O, l);
     return launched("merge");
+}
+
+dfa_status launch_merge_pieces(dfa_dtype dt, int B, int H, int S, int D, int causal, int piece_tiles,
+                               int n_split, const float* O_part, const float* lse_part, void* O, float* lse,
+                               cudaStream_t s) {
+    const int64_t rows = (int64_t)B * S * H;
+    if (rows == 0) return DFA_OK;
+    if (piece_tiles <= 0 || n_split <= 0 || D % 4 != 0) return fail(DFA_ERR_INVALID_ARG, "bad split-kv merge sizes");
+    const int64_t blocks = (rows + kThreads / 32 - 1) / (kThreads / 32);
+    if (dt == DFA_F32)
+        merge_pieces_kernel<float><<<(unsigned)blocks, kThreads, 0, s>>>(B, H, S, D, causal, piece_tiles, n_split,
+                                                                         O_part, lse_part, (float*)O, lse);
+    else
+        merge_pieces_kernel<__nv_bfloat16><<<(unsigned)blocks, kThreads, 0, s>>>(
+            B, H, S, D, causal, piece_tiles, n_split, O_part, lse_part, (__nv_bfloat16*)O, lse);
+    return launched("split-kv merge");
 }
 
 dfa_status launch_delta(dfa_dtype dt, int B, int H, int S, int D, const void* O,

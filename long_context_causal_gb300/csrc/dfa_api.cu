@@ -54,6 +54,7 @@ std::map<std::tuple<int, int, int, int>, CachedList> g_lists;
 
 // Returns the pinned host copy of the list (nullptr on failure).
 const CachedList* get_list(int rows, int units, int workers, dfa_sched sched) {
+    if (sched == DFA_SCHED_SPLIT_KV) sched = DFA_SCHED_BALANCED;   // pieces are listed by get_split_list
     std::lock_guard<std::mutex> lk(g_mu);
     auto key = std::make_tuple(rows, units, workers, (int)sched);
     auto it = g_lists.find(key);
@@ -71,9 +72,42 @@ const CachedList* get_list(int rows, int units, int workers, dfa_sched sched) {
     return &(g_lists[key] = c);
 }
 
+// Split-kv pieces of a forward (dfa_build_split_worklist), cached like the
+// plain lists; key (rows, units, kv_tiles, causal, piece_tiles, workers).
+std::map<std::tuple<int, int, int, int, int, int>, CachedList> g_split_lists;
+
+int64_t count_pieces(int rows, int units, int kv_tiles, int causal, int piece) {
+    int64_t n = 0;
+    for (int u = 0; u < units; ++u) {
+        const int hi = causal ? std::min(2 * u + 2, kv_tiles) : kv_tiles;
+        n += (hi + piece - 1) / piece;
+    }
+    return n * rows;
+}
+
+const CachedList* get_split_list(int rows, int units, int kv_tiles, int causal, int piece, int workers) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto key = std::make_tuple(rows, units, kv_tiles, causal, piece, workers);
+    auto it = g_split_lists.find(key);
+    if (it != g_split_lists.end()) return &it->second;
+    const int64_t n = count_pieces(rows, units, kv_tiles, causal, piece);
+    CachedList c;
+    c.count = (size_t)workers + 1 + (size_t)n;
+    c.workers = workers;
+    if (cudaHostAlloc((void**)&c.host, c.count * sizeof(int32_t), cudaHostAllocDefault) != cudaSuccess)
+        return nullptr;
+    if (dfa_build_split_worklist(rows, units, kv_tiles, causal, piece, workers, c.host, c.host + workers + 1) < 0 ||
+        c.host[workers] != n) {
+        cudaFreeHost(c.host);
+        return nullptr;
+    }
+    return &(g_split_lists[key] = c);
+}
+
 struct Layout {
-    size_t delta = 0, lse2 = 0, dq = 0, wl = 0, total = 0;
+    size_t delta = 0, lse2 = 0, dq = 0, wl = 0, opart = 0, lpart = 0, total = 0;
     int S_pad = 0;
+    int n_split = 1;   // forward: split-kv pieces the workspace has room for
 };
 
 Layout layout(int B, int H, int Hkv, int S, int D, bool bwd) {
@@ -92,7 +126,19 @@ Layout layout(int B, int H, int Hkv, int S, int D, bool bwd) {
     const size_t units = bwd ? (size_t)(S + kBwdUnitRows - 1) / kBwdUnitRows
                              : (size_t)(S + kFwdUnitRows - 1) / kFwdUnitRows;
     const size_t rows = bwd ? (size_t)B * Hkv : (size_t)B * H;
-    off = align_up(off + sizeof(int32_t) * (kMaxWorkers + 1 + rows * units));
+    if (!bwd) {
+        // Room for SPLIT_KV pieces when the problem is small enough to be split;
+        // the causal plan has the shortest pieces, so it bounds both masks.
+        const int piece = dfa_split_piece_tiles(B, H, S, 1, num_sms());
+        if (piece > 0) L.n_split = (int)(((S + 127) / 128 + piece - 1) / piece);
+    }
+    off = align_up(off + sizeof(int32_t) * (kMaxWorkers + 1 + rows * units * (size_t)L.n_split));
+    if (L.n_split > 1) {
+        L.opart = off;
+        off = align_up(off + sizeof(float) * (size_t)L.n_split * B * S * H * D);
+        L.lpart = off;
+        off = align_up(off + sizeof(float) * (size_t)L.n_split * B * H * S);
+    }
     L.total = off;
     return L;
 }
@@ -253,7 +299,7 @@ static dfa_status check_whole(dfa_dtype dt, int B, int H, int H_kv, int S, int D
     if (S < 0) return fail(DFA_ERR_INVALID_ARG, "negative sequence length");
     if (n_chunks <= 0 || S % n_chunks != 0)
         return fail(DFA_ERR_INVALID_ARG, "S=%d must split into n_chunks=%d equal chunks", S, n_chunks);
-    if (sched != DFA_SCHED_BALANCED && sched != DFA_SCHED_UNBALANCED)
+    if (sched != DFA_SCHED_BALANCED && sched != DFA_SCHED_UNBALANCED && sched != DFA_SCHED_SPLIT_KV)
         return fail(DFA_ERR_INVALID_ARG, "unknown schedule %d", (int)sched);
     if ((int64_t)B * S == 0) return DFA_OK;
     const size_t need = layout(B, H, H_kv, S, D, bwd).total;
@@ -298,6 +344,29 @@ static dfa_status attn_fwd_impl(const void* q, const void* k, const void* v, dfa
     } else {
         const Layout L = layout(B, H, H_kv, S, D, false);
         const int units = (S + kFwdUnitRows - 1) / kFwdUnitRows;
+        const int piece = sched == DFA_SCHED_SPLIT_KV && !window ? dfa_split_piece_tiles(B, H, S, causal, num_sms()) : 0;
+        if (piece > 0) {
+            // Helper items: pieces of every block's key range, partials to the
+            // workspace, then the rescale-and-merge of each row's pieces.
+            const int kv_tiles = (S + 127) / 128, n_split = (kv_tiles + piece - 1) / piece;
+            if (n_split > L.n_split) return fail(DFA_ERR_WORKSPACE, "split-kv plan exceeds the workspace layout");
+            const int64_t n = count_pieces(B * H, units, kv_tiles, causal != 0, piece);
+            const int workers = (int)std::min<int64_t>(num_sms(), n);
+            const CachedList* c = get_split_list(B * H, units, kv_tiles, causal != 0, piece, workers);
+            if (!c) return fail(DFA_ERR_CUDA, "could not build the split-kv work list");
+            int32_t* dev = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + L.wl);
+            if ((st = upload_list(c, dev, s))) return st;
+            WorkList wl{dev, dev + workers + 1, workers, units};
+            wl.n_split = n_split;
+            wl.piece_tiles = piece;
+            float* opart = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.opart);
+            float* lpart = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.lpart);
+            if ((st = tc_fwd(p, q, k, v, opart, true, lpart, &wl, s))) return st;
+            count_launch(DFA_KERNEL_FWD);
+            st = launch_merge_pieces(dt, B, H, S, D, causal != 0, piece, n_split, opart, lpart, O, lse, s);
+            if (st == DFA_OK) count_launch(DFA_KERNEL_MERGE);
+            return st;
+        }
         const int workers = std::min(num_sms(), B * H * units);
         const CachedList* c = get_list(B * H, units, workers, sched);
         if (!c) return fail(DFA_ERR_CUDA, "could not build the work list");

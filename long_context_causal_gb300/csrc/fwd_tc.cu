@@ -68,6 +68,11 @@ struct FwdArgs {
     const int32_t* wl_offsets;
     const int32_t* wl_items;
     int n_units;
+    // Split-kv helper items: item values carry a piece index s < n_split and
+    // see key tiles [s * piece_tiles, (s + 1) * piece_tiles) only; piece s
+    // writes its partial to O + s * o_piece_stride, lse + s * lse_piece_stride.
+    int n_split, piece_tiles;
+    int64_t o_piece_stride, lse_piece_stride;
     int* err;
     uint64_t* trace;              // optional per-CTA timeline (nullptr: off)
     int trace_cap;
@@ -75,6 +80,7 @@ struct FwdArgs {
 
 struct Item {
     int b, h, g, q0, j0, n_kv;   // key/value tiles [j0, n_kv) can be visible to the block
+    int s;                       // key/value piece (0 without split-kv items)
 };
 
 // First key position a query at position qp may see under the local window.
@@ -84,6 +90,11 @@ __device__ __forceinline__ int64_t window_lo(const FwdArgs& a, int64_t qp) {
 
 __device__ __forceinline__ Item decode(const FwdArgs& a, int it, bool win) {
     Item x;
+    x.s = 0;
+    if (a.n_split > 1) {
+        x.s = it % a.n_split;
+        it /= a.n_split;
+    }
     const int row = it / a.n_units, unit = it % a.n_units;
     x.b = row / a.H;
     x.h = row % a.H;
@@ -102,6 +113,11 @@ __device__ __forceinline__ Item decode(const FwdArgs& a, int it, bool win) {
     if (win) {   // the block's first row has the lowest window start
         const int64_t lo = window_lo(a, a.q_offset + x.q0) - a.kv_offset;
         x.j0 = lo <= 0 ? 0 : (int)(lo / BN < x.n_kv ? lo / BN : x.n_kv);
+    }
+    if (a.n_split > 1) {   // this piece's tiles only (an empty range does no MMA work)
+        const int lo = x.s * a.piece_tiles, hi = lo + a.piece_tiles;
+        x.j0 = max(x.j0, lo);
+        x.n_kv = max(min(x.n_kv, hi), x.j0);
     }
     return x;
 }
@@ -424,7 +440,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             // ---- epilogue: O = O_acc / l, lse = ln(sum exp(s))
             const bool valid_row = row < a.Lq;
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            const int64_t orow = (((int64_t)x.b * a.Lq + row) * a.H + x.h) * D;
+            const int64_t orow = (((int64_t)x.b * a.Lq + row) * a.H + x.h) * D + x.s * a.o_piece_stride;
             if (x.n_kv > x.j0) {
                 ok = __all_sync(0xffffffffu, mbar_wait_acc(&o_full[w], qi & 1, abort_flag, a.err, nullptr));
                 if (!ok) break;
@@ -464,7 +480,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 }
             }
             if (valid_row)
-                a.lse[((int64_t)x.b * a.H + x.h) * a.Lq + row] = l > 0.f ? (m_run + __log2f(l)) * kLn2 : -INFINITY;
+                a.lse[((int64_t)x.b * a.H + x.h) * a.Lq + row + x.s * a.lse_piece_stride] = l > 0.f ? (m_run + __log2f(l)) * kLn2 : -INFINITY;
         }
         if (threadIdx.x == 128) trace_count(a.trace, a.trace_cap, 5, t);
     }
@@ -534,10 +550,18 @@ static dfa_status launch(const AttnProblem& p, const void* q, const void* k, con
     a.err = device_error_flag();
     a.trace = cta_trace(&a.trace_cap);
     int grid;
+    a.n_split = 1;
     if (wl) {
         a.wl_offsets = wl->offsets;
         a.wl_items = wl->items;
         grid = wl->n_workers;
+        if (wl->n_split > 1) {
+            if (!OUT_F32 || wl->piece_tiles <= 0) return fail(DFA_ERR_INVALID_ARG, "split-kv pieces need fp32 partials");
+            a.n_split = wl->n_split;
+            a.piece_tiles = wl->piece_tiles;
+            a.o_piece_stride = (int64_t)p.B * p.Lq * p.H * D;
+            a.lse_piece_stride = (int64_t)p.B * p.H * p.Lq;
+        }
     } else {
         a.wl_offsets = nullptr;
         a.wl_items = nullptr;

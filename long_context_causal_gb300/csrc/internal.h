@@ -44,6 +44,13 @@ dfa_status simt_bwd(const AttnProblem& p, dfa_dtype dt, const void* q, const voi
 // ---- small HBM-bound kernels (aux_kernels.cu) ----
 dfa_status launch_merge(int B, int H, int L, int D, const float* Oa, const float* la,
                         const float* Ob, const float* lb, float* O, float* l, cudaStream_t s);
+// Merge of the split-kv pieces of a whole-sequence forward: row i of query
+// block u = i / 256 has pieces s < ceil(hi(u) / piece_tiles) (hi as in
+// dfa_build_split_worklist) in O_part [n_split][B, S, H, D] fp32 and
+// lse_part [n_split][B, H, S]; writes O [B, S, H, D] in dt and lse [B, H, S].
+dfa_status launch_merge_pieces(dfa_dtype dt, int B, int H, int S, int D, int causal, int piece_tiles,
+                               int n_split, const float* O_part, const float* lse_part, void* O, float* lse,
+                               cudaStream_t s);
 // Delta[b,h,i] = sum_d dO[b,i,h,d] * O[b,i,h,d]   (dense BSHD, fp32 out [B,H,S]).
 dfa_status launch_delta(dfa_dtype dt, int B, int H, int S, int D, const void* O,
                         const void* dO, float* delta, cudaStream_t s);
@@ -63,7 +70,13 @@ struct WorkList {
     const int32_t* items;    // [n_items], device: row * n_units + unit
     int n_workers;
     int n_units;
+    // Forward split-kv items (dfa_build_split_worklist): values are
+    // (row * n_units + unit) * n_split + piece; 1 / 0 without pieces.
+    int n_split = 1;
+    int piece_tiles = 0;
 };
+// With split-kv items (wl->n_split > 1) O must be fp32: piece s of every row
+// goes to O + s * B*Lq*H*D and lse + s * B*H*Lq.
 dfa_status tc_fwd(const AttnProblem& p, const void* q, const void* k, const void* v, void* O,
                   bool O_is_f32, float* lse, const WorkList* wl, cudaStream_t s);
 // lse2 = lse * log2(e) and delta are [B, H, S_pad] (S_pad = S rounded up to 128,

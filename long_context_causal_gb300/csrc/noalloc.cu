@@ -114,8 +114,9 @@ extern "C" dfa_status dfa_attn_fwd_noalloc(const void* q, const void* k, const v
     if (!(scale > 0.f) || !std::isfinite(scale)) return fail(DFA_ERR_INVALID_ARG, "scale must be finite and > 0");
     if (n_chunks <= 0 || S % n_chunks != 0)
         return fail(DFA_ERR_INVALID_ARG, "S=%d must split into n_chunks=%d equal chunks", S, n_chunks);
-    if (sched != DFA_SCHED_BALANCED && sched != DFA_SCHED_UNBALANCED)
+    if (sched != DFA_SCHED_BALANCED && sched != DFA_SCHED_UNBALANCED && sched != DFA_SCHED_SPLIT_KV)
         return fail(DFA_ERR_INVALID_ARG, "unknown schedule %d", (int)sched);
+    if (sched == DFA_SCHED_SPLIT_KV) sched = DFA_SCHED_BALANCED;   // no workspace for pieces
     if ((int64_t)B * S == 0) return DFA_OK;
     const int64_t rows = (int64_t)B * H, units = (S + kUnitRows - 1) / kUnitRows;
     if (kNoAllocMaxWorkers + 1 + rows * units > kNoAllocEntries)

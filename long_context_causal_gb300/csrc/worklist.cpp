@@ -9,6 +9,9 @@
 // workers: 36 blocks in 8 steps (4.5x) unbalanced, in 5 steps (7.2x) balanced.
 #include <algorithm>
 #include <cstdint>
+#include <functional>
+#include <queue>
+#include <utility>
 #include <vector>
 
 #include "../../include/dfa.h"
@@ -61,6 +64,74 @@ extern "C" int64_t dfa_build_worklist(int n_rows, int n_units, int n_workers, df
         offsets[w] = (int32_t)pos;
         for (int32_t it : per[w]) items[pos++] = it;
         makespan = std::max(makespan, cost[w]);
+    }
+    offsets[W] = (int32_t)pos;
+    return makespan;
+}
+
+namespace {
+
+// Key tiles a forward query block sees: [0, hi(u)).
+inline int64_t block_hi(int64_t u, int64_t kv_tiles, int causal) {
+    return causal ? std::min(2 * u + 2, kv_tiles) : kv_tiles;
+}
+
+}  // namespace
+
+extern "C" int dfa_split_piece_tiles(int B, int H, int S, int causal, int n_sms) {
+    if (B <= 0 || H <= 0 || S <= 0 || n_sms <= 0) return 0;
+    const int64_t units = (S + 255) / 256, kv_tiles = (S + 127) / 128;
+    const int64_t rows = (int64_t)B * H;
+    if (rows * units >= n_sms) return 0;   // every SM already has a query block
+    int64_t work = 0;                      // key tiles over all blocks
+    for (int64_t u = 0; u < units; ++u) work += block_hi(u, kv_tiles, causal);
+    work *= rows;
+    // About two pieces per SM so the greedy deal can even out the causal
+    // triangle; at least four tiles so a piece amortises its Q load and its
+    // fp32 partial store.
+    const int64_t piece = std::max<int64_t>(4, (work + 2 * n_sms - 1) / (2 * n_sms));
+    if ((kv_tiles + piece - 1) / piece <= 1) return 0;
+    return (int)piece;
+}
+
+extern "C" int64_t dfa_build_split_worklist(int n_rows, int n_units, int kv_tiles, int causal, int piece_tiles,
+                                            int n_workers, int32_t* offsets, int32_t* items) {
+    if (n_rows < 0 || n_units < 0 || kv_tiles < 0 || piece_tiles <= 0 || n_workers <= 0 || !offsets) return -1;
+    const int64_t n_split = std::max<int64_t>(1, (kv_tiles + piece_tiles - 1) / piece_tiles);
+    if ((int64_t)n_rows * n_units * n_split > INT32_MAX) return -1;
+    struct Piece {
+        int64_t cost;
+        int32_t value;
+    };
+    std::vector<Piece> pieces;
+    for (int64_t row = 0; row < n_rows; ++row)
+        for (int64_t u = 0; u < n_units; ++u) {
+            const int64_t hi = block_hi(u, kv_tiles, causal);
+            for (int64_t s = 0; s * piece_tiles < hi; ++s) {
+                const int64_t len = std::min<int64_t>(hi, (s + 1) * piece_tiles) - s * piece_tiles;
+                pieces.push_back({2 * len, (int32_t)((row * n_units + u) * n_split + s)});
+            }
+        }
+    if (!pieces.empty() && !items) return -1;
+    std::stable_sort(pieces.begin(), pieces.end(), [](const Piece& x, const Piece& y) { return x.cost > y.cost; });
+    const int64_t W = n_workers;
+    std::vector<std::vector<int32_t>> per(W);
+    using Load = std::pair<int64_t, int64_t>;   // (cost so far, worker): the smallest first
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+    for (int64_t w = 0; w < W; ++w) heap.push({0, w});
+    int64_t makespan = 0;
+    for (const Piece& pc : pieces) {
+        Load l = heap.top();
+        heap.pop();
+        per[l.second].push_back(pc.value);
+        l.first += pc.cost;
+        makespan = std::max(makespan, l.first);
+        heap.push(l);
+    }
+    int64_t pos = 0;
+    for (int64_t w = 0; w < W; ++w) {
+        offsets[w] = (int32_t)pos;
+        for (int32_t it : per[w]) items[pos++] = it;
     }
     offsets[W] = (int32_t)pos;
     return makespan;

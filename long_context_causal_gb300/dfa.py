@@ -23,10 +23,11 @@ HEADER = os.path.join(INCLUDE, "dfa.h")
 
 DFA_OK, DFA_ERR_INVALID_ARG, DFA_ERR_UNSUPPORTED, DFA_ERR_CUDA, DFA_ERR_TIMEOUT, DFA_ERR_WORKSPACE = range(6)
 DFA_F32, DFA_BF16 = 0, 1
-DFA_SCHED_BALANCED, DFA_SCHED_UNBALANCED = 0, 1
+DFA_SCHED_BALANCED, DFA_SCHED_UNBALANCED, DFA_SCHED_SPLIT_KV = 0, 1, 2
 KERNEL_KINDS = {"fwd": 0, "bwd": 1, "merge": 2, "delta": 3, "convert": 4}
-_SCHED = {"balanced": DFA_SCHED_BALANCED, "unbalanced": DFA_SCHED_UNBALANCED,
-          DFA_SCHED_BALANCED: DFA_SCHED_BALANCED, DFA_SCHED_UNBALANCED: DFA_SCHED_UNBALANCED}
+_SCHED = {"balanced": DFA_SCHED_BALANCED, "unbalanced": DFA_SCHED_UNBALANCED, "split_kv": DFA_SCHED_SPLIT_KV,
+          DFA_SCHED_BALANCED: DFA_SCHED_BALANCED, DFA_SCHED_UNBALANCED: DFA_SCHED_UNBALANCED,
+          DFA_SCHED_SPLIT_KV: DFA_SCHED_SPLIT_KV}
 
 
 class DfaError(RuntimeError):
@@ -61,6 +62,8 @@ def _load() -> ctypes.CDLL:
         "dfa_launch_count": (i64, [i32]),
         "dfa_build_worklist": (i64, [i32, i32, i32, i32, p32, p32]),
         "dfa_chunk_schedule": (i32, [i32, i32, i32, p32]),
+        "dfa_split_piece_tiles": (i32, [i32, i32, i32, i32, i32]),
+        "dfa_build_split_worklist": (i64, [i32, i32, i32, i32, i32, i32, p32, p32]),
         "dfa_debug_mma": (i32, [i32, vp, vp, vp, vp]),
         "dfa_debug_cta_trace": (i32, [vp, i32]),
     }
@@ -320,6 +323,26 @@ def dfa_build_worklist(n_rows: int, n_units: int, n_workers: int, sched="balance
     if mk < 0:
         raise DfaError(DFA_ERR_INVALID_ARG, "bad work-list arguments")
     return offsets, items[: n_rows * n_units], int(mk)
+
+
+def dfa_split_piece_tiles(B: int, H: int, S: int, causal: bool, n_sms: int) -> int:
+    """Host-only: the split-kv piece length (128-key tiles) for this problem, 0 if not split."""
+    return int(_lib.dfa_split_piece_tiles(B, H, S, int(bool(causal)), n_sms))
+
+
+def dfa_build_split_worklist(n_rows: int, n_units: int, kv_tiles: int, causal: bool, piece_tiles: int,
+                             n_workers: int):
+    """Host-only: split-kv pieces dealt to workers -> (offsets, items, makespan)."""
+    import numpy as np
+    n_split = max(1, -(-kv_tiles // piece_tiles)) if piece_tiles > 0 else 1
+    offsets = np.zeros(n_workers + 1, dtype=np.int32)
+    items = np.zeros(max(n_rows * n_units * n_split, 1), dtype=np.int32)
+    p32 = ctypes.POINTER(ctypes.c_int32)
+    mk = _lib.dfa_build_split_worklist(n_rows, n_units, kv_tiles, int(bool(causal)), piece_tiles, n_workers,
+                                       offsets.ctypes.data_as(p32), items.ctypes.data_as(p32))
+    if mk < 0:
+        raise DfaError(DFA_ERR_INVALID_ARG, "bad split work-list arguments")
+    return offsets, items[: offsets[-1]], int(mk)
 
 
 def dfa_chunk_schedule(P: int, sched="balanced"):

@@ -82,3 +82,65 @@ def test_balanced_worklist_beats_unbalanced_makespan():
 def test_worklist_rejects_bad_arguments():
     with pytest.raises(dfa.DfaError):
         dfa.dfa_build_worklist(1, 4, 0)
+
+
+# ---------------------------------------------------------------- split-kv helper items
+def _hi(u, kv_tiles, causal):
+    return min(2 * u + 2, kv_tiles) if causal else kv_tiles
+
+
+@pytest.mark.parametrize("B,H,S,causal,n_sms", [(1, 1, 4096, True, 152), (1, 2, 8192, True, 152),
+                                                (1, 1, 1000, True, 152), (1, 2, 2048, False, 152),
+                                                (2, 3, 1536, True, 148), (1, 1, 32768, True, 152)])
+def test_split_piece_tiles_gives_at_least_two_pieces_of_four_tiles(B, H, S, causal, n_sms):
+    piece = dfa.dfa_split_piece_tiles(B, H, S, causal, n_sms)
+    kv_tiles = -(-S // 128)
+    assert piece >= 4
+    assert -(-kv_tiles // piece) >= 2
+    units = -(-S // 256)
+    work = B * H * sum(_hi(u, kv_tiles, causal) for u in range(units))
+    assert piece == max(4, -(-work // (2 * n_sms)))
+
+
+@pytest.mark.parametrize("B,H,S,n_sms", [(1, 152, 4096, 152), (32, 32, 131072, 152), (1, 1, 256, 152),
+                                         (1, 1, 384, 152), (0, 4, 1024, 152), (1, 4, 1024, 0)])
+def test_split_is_not_used_when_every_sm_has_a_block_or_nothing_gains(B, H, S, n_sms):
+    assert dfa.dfa_split_piece_tiles(B, H, S, True, n_sms) == 0
+
+
+@pytest.mark.parametrize("rows,units,kv_tiles,causal,piece,W", [
+    (1, 16, 32, True, 4, 152), (2, 32, 64, True, 7, 152), (1, 4, 8, True, 4, 10), (2, 8, 16, False, 4, 32),
+    (6, 6, 12, True, 4, 36), (1, 128, 256, True, 55, 152), (3, 5, 9, True, 3, 7), (1, 1, 1, True, 4, 1)])
+def test_split_worklist_covers_every_visible_tile_once(rows, units, kv_tiles, causal, piece, W):
+    offsets, items, makespan = dfa.dfa_build_split_worklist(rows, units, kv_tiles, causal, piece, W)
+    n_split = -(-kv_tiles // piece)
+    assert offsets[0] == 0 and np.all(np.diff(offsets) >= 0) and offsets[-1] == len(items)
+    assert len(set(items.tolist())) == len(items)
+    seen = {}
+    cost = []
+    for w in range(W):
+        c = 0
+        for it in items[offsets[w]:offsets[w + 1]]:
+            s, ru = int(it) % n_split, int(it) // n_split
+            row, u = ru // units, ru % units
+            assert 0 <= row < rows
+            hi = _hi(u, kv_tiles, causal)
+            lo, top = s * piece, min((s + 1) * piece, hi)
+            assert lo < top, "empty pieces are not listed"
+            for j in range(lo, top):
+                key = (row, u, j)
+                assert key not in seen
+                seen[key] = w
+            c += 2 * (top - lo)
+        cost.append(c)
+    expect = {(r, u, j) for r in range(rows) for u in range(units) for j in range(_hi(u, kv_tiles, causal))}
+    assert set(seen) == expect
+    assert makespan == max(cost)
+    # Longest-first greedy: no worker ends more than one piece above the average.
+    assert makespan <= sum(cost) / W + 2 * piece
+
+
+def test_split_worklist_rejects_bad_arguments():
+    for args in [(1, 4, 8, True, 0, 4), (1, 4, 8, True, 4, 0), (-1, 4, 8, True, 4, 4)]:
+        with pytest.raises(dfa.DfaError):
+            dfa.dfa_build_split_worklist(*args)
