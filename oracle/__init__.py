@@ -11,7 +11,9 @@ module compiles it with gcc and marshals numpy arrays.  What is computed, and
 the passages it follows, is documented at the top of ``oracle.c``:
 DISTFLASHATTN (paperlayer.ai summary of arXiv 2310.03294) §3.1, §3.2, §3.3 and
 App. D, with the online-normalizer merge rule of "Online normalizer
-calculation for softmax".
+calculation for softmax".  ``attn_fwd_varlen`` / ``attn_bwd_varlen`` apply
+the same definition to a packed batch of sequences of different lengths, one
+sequence at a time (no token attends across a sequence boundary).
 
 Parity status: every function here is pinned by ``tests/test_oracle.py``
 (finite differences, closed forms, invariants, a library special case and
@@ -237,3 +239,47 @@ def merge(O_a, lse_a, O_b, lse_b):
     rc = _load().oracle_merge(_p(O_a), _p(lse_a), _p(O_b), _p(lse_b), B, H, L, D, _p(O), _p(lse))
     _check(rc, "merge")
     return O, lse
+
+
+def _cu(cu_seqlens, T):
+    cu = np.asarray(cu_seqlens, dtype=np.int64).reshape(-1)
+    if cu.size < 1 or cu[0] != 0 or cu[-1] != T or np.any(np.diff(cu) < 0):
+        raise ValueError("cu_seqlens must start at 0, never decrease and end at the packed length")
+    return cu
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens, *, causal=True, scale=None, threads=0):
+    """Variable-length batch packed along the token axis: q [T, H, D], k, v
+    [T, H_kv, D]; sequence s holds tokens [cu[s], cu[s+1]) and attends only to
+    its own tokens (causal inside the sequence when causal).  Returns O [T, H, D]
+    and lse [H, T].  Attention of one sequence never reads another, so the
+    result is the plain attention of every sequence on its own."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    T, H, D = q.shape
+    cu = _cu(cu_seqlens, T)
+    O = np.zeros_like(q)
+    lse = np.zeros((H, T))
+    for s in range(cu.size - 1):
+        a, b = int(cu[s]), int(cu[s + 1])
+        if a == b:
+            continue
+        Os, ls = attn_fwd(q[None, a:b], k[None, a:b], v[None, a:b], causal=causal, scale=scale, threads=threads)
+        O[a:b] = Os[0]
+        lse[:, a:b] = ls[0]
+    return O, lse
+
+
+def attn_bwd_varlen(q, k, v, dO, cu_seqlens, *, causal=True, scale=None, threads=0):
+    """dQ [T, H, D], dK, dV [T, H_kv, D] of attn_fwd_varlen."""
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    T = q.shape[0]
+    cu = _cu(cu_seqlens, T)
+    dQ, dK, dV = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for s in range(cu.size - 1):
+        a, b = int(cu[s]), int(cu[s + 1])
+        if a == b:
+            continue
+        g = attn_bwd(q[None, a:b], k[None, a:b], v[None, a:b], dO[None, a:b], causal=causal, scale=scale,
+                     threads=threads)
+        dQ[a:b], dK[a:b], dV[a:b] = g[0][0], g[1][0], g[2][0]
+    return dQ, dK, dV

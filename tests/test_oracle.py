@@ -362,3 +362,81 @@ def test_golden_fixture_reproduces():
     dQ, dK, dV = oracle.attn_bwd(q, k, v, dO, scale=fx["scale"])
     for name, got in (("O", O), ("lse", lse), ("dQ", dQ), ("dK", dK), ("dV", dV)):
         np.testing.assert_allclose(got, np.array(fx[name]), atol=1e-14, err_msg=name)
+
+
+# ---------------------------------------------------------------- variable-length batches
+def block_mask(cu, causal):
+    """Allowed (query, key) pairs of a packed batch: same sequence, and key <= query when causal."""
+    T = int(cu[-1])
+    seq = np.searchsorted(np.asarray(cu), np.arange(T), side="right") - 1
+    allow = seq[:, None] == seq[None, :]
+    if causal:
+        allow &= np.arange(T)[None, :] <= np.arange(T)[:, None]
+    return allow
+
+
+@pytest.mark.parametrize("lens,H,Hkv,causal", [([5, 0, 9, 1, 13], 4, 2, True), ([7, 7, 3], 2, 2, False),
+                                               ([1], 3, 1, True), ([16, 2, 0], 2, 1, True)])
+def test_varlen_matches_torch_sdpa_with_a_block_diagonal_mask(lens, H, Hkv, causal):
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    T, D, scale = int(cu[-1]), 8, 0.37
+    q, k, v, dO = rnd((T, H, D), 120), rnd((T, Hkv, D), 121), rnd((T, Hkv, D), 122), rnd((T, H, D), 123)
+    O, lse = oracle.attn_fwd_varlen(q, k, v, cu, causal=causal, scale=scale)
+    dQ, dK, dV = oracle.attn_bwd_varlen(q, k, v, dO, cu, causal=causal, scale=scale)
+    G = H // Hkv
+    tq = torch.tensor(q).transpose(0, 1)[None].requires_grad_()
+    tk = torch.tensor(k).transpose(0, 1)[None].requires_grad_()
+    tv = torch.tensor(v).transpose(0, 1)[None].requires_grad_()
+    kk, vv = tk.repeat_interleave(G, dim=1), tv.repeat_interleave(G, dim=1)
+    allow = torch.tensor(block_mask(cu, causal))
+    out = torch.nn.functional.scaled_dot_product_attention(tq, kk, vv, attn_mask=allow, scale=scale)
+    out.backward(torch.tensor(dO).transpose(0, 1)[None])
+    np.testing.assert_allclose(O, out.detach()[0].transpose(0, 1).numpy(), atol=1e-12)
+    np.testing.assert_allclose(dQ, tq.grad[0].transpose(0, 1).numpy(), atol=1e-11)
+    np.testing.assert_allclose(dK, tk.grad[0].transpose(0, 1).numpy(), atol=1e-11)
+    np.testing.assert_allclose(dV, tv.grad[0].transpose(0, 1).numpy(), atol=1e-11)
+    s = scale * torch.einsum("hid,hjd->hij", tq.detach()[0], kk.detach()[0])
+    s = s.masked_fill(~allow, float("-inf"))
+    np.testing.assert_allclose(lse, torch.logsumexp(s, dim=-1).numpy(), atol=1e-12)
+
+
+def test_varlen_of_equal_lengths_is_the_dense_batch():
+    n, L, H, Hkv, D = 3, 11, 4, 2, 6
+    q, k, v, dO = rnd((n, L, H, D), 130), rnd((n, L, Hkv, D), 131), rnd((n, L, Hkv, D), 132), rnd((n, L, H, D), 133)
+    cu = np.arange(n + 1) * L
+    O, lse = oracle.attn_fwd_varlen(q.reshape(n * L, H, D), k.reshape(n * L, Hkv, D), v.reshape(n * L, Hkv, D), cu)
+    Od, ld = oracle.attn_fwd(q, k, v)
+    np.testing.assert_array_equal(O.reshape(n, L, H, D), Od)
+    np.testing.assert_array_equal(lse.reshape(H, n, L).transpose(1, 0, 2), ld)
+    g = oracle.attn_bwd_varlen(*(x.reshape(n * L, x.shape[2], D) for x in (q, k, v, dO)), cu)
+    gd = oracle.attn_bwd(q, k, v, dO)
+    for a, b in zip(g, gd):   # same sums, possibly another order across the batch
+        np.testing.assert_allclose(a.reshape(b.shape), b, rtol=0, atol=1e-13)
+
+
+def test_varlen_gradients_match_finite_differences():
+    cu = np.array([0, 3, 3, 7])
+    T, H, Hkv, D = 7, 2, 1, 2
+    q, k, v, dO = rnd((T, H, D), 140), rnd((T, Hkv, D), 141), rnd((T, Hkv, D), 142), rnd((T, H, D), 143)
+    dQ, dK, dV = oracle.attn_bwd_varlen(q, k, v, dO, cu, scale=0.9)
+    h = 1e-6
+    for name, x, g in (("q", q, dQ), ("k", k, dK), ("v", v, dV)):
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(*x.shape):
+            vals = []
+            for sgn in (1, -1):
+                args = {"q": q, "k": k, "v": v}
+                xx = x.copy()
+                xx[idx] += sgn * h
+                args[name] = xx
+                O, _ = oracle.attn_fwd_varlen(args["q"], args["k"], args["v"], cu, scale=0.9)
+                vals.append(float(np.sum(O * dO)))
+            fd[idx] = (vals[0] - vals[1]) / (2 * h)
+        assert np.max(np.abs(fd - g) / np.maximum(1.0, np.abs(g))) < 1e-7, name
+
+
+def test_varlen_rejects_bad_offsets():
+    q = rnd((4, 1, 2), 150)
+    for cu in ([0, 3], [1, 4], [0, 3, 2, 4]):
+        with pytest.raises(ValueError):
+            oracle.attn_fwd_varlen(q, q, q, cu)
