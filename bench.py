@@ -45,6 +45,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-chunk-step", action="store_true", help="skip the per-worker chunk-step timing")
     ap.add_argument("--window", type=int, default=2, help="chunks per local window for the extra local-window timing (0: skip)")
+    ap.add_argument("--no-varlen", action="store_true", help="skip the packed-batch timing")
     ap.add_argument("--no-split-kv", action="store_true", help="skip the small-problem split-kv forward timing")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target oracle sample time")
     return ap.parse_args()
@@ -362,6 +363,68 @@ def split_kv_timing(device, stream, dfa, reps=10):
     return out
 
 
+VARLEN_LENS = [57344, 28672, 16384, 12288, 8192, 4096, 2048, 1024, 512, 512]   # 131072 tokens
+
+
+def varlen_timing(device, stream, dfa, H=32, Hkv=32, D=128, reps=3):
+    """A packed batch of sequences of very different lengths (a long-tail mix of
+    128K tokens at the Llama-7B head shape): causal forward + backward as one
+    launch each through the packed entry points, against one dense call per
+    sequence.  FLOPs on each sequence's own causal triangle.  Each packed
+    tensor (1 GB) exceeds L2.  Reported beside the headline."""
+    import numpy as np
+    import torch
+    from long_context_causal_gb300.inputs import make
+    lens = VARLEN_LENS
+    T = sum(lens)
+    q, k, v, do = (x[0] for x in make(1, H, Hkv, T, D, torch.bfloat16, seed=5, device=device))
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    O = torch.empty_like(q)
+    lse = torch.empty((H, T), dtype=torch.float32, device=device)
+    dQ, dK, dV = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    wsf = dfa.varlen_workspace(cu, H, Hkv, D, False, device)
+    wsb = dfa.varlen_workspace(cu, H, Hkv, D, True, device)
+    pairs = sum(L * (L + 1) // 2 for L in lens) * H
+    segs = [(int(a), int(b)) for a, b in zip(cu[:-1], cu[1:])]
+    seg_lse = [torch.empty((1, H, b - a), dtype=torch.float32, device=device) for a, b in segs]
+    wsd = {b - a: (dfa.workspace(1, H, Hkv, b - a, D, 1, False, device),
+                   dfa.workspace(1, H, Hkv, b - a, D, 1, True, device)) for a, b in segs}
+
+    def packed_fwd():
+        dfa.dfa_attn_fwd_varlen(q, k, v, cu, O=O, lse=lse, workspace_buf=wsf, stream=stream)
+
+    def packed_bwd():
+        dfa.dfa_attn_bwd_varlen(q, k, v, O, lse, do, cu, dQ=dQ, dK=dK, dV=dV, workspace_buf=wsb, stream=stream)
+
+    def loop_fwd():
+        for (a, b), l in zip(segs, seg_lse):
+            dfa.dfa_attn_fwd(q[None, a:b], k[None, a:b], v[None, a:b], O=O[None, a:b], lse=l,
+                             workspace_buf=wsd[b - a][0], stream=stream)
+
+    def loop_bwd():
+        for (a, b), l in zip(segs, seg_lse):
+            dfa.dfa_attn_bwd(q[None, a:b], k[None, a:b], v[None, a:b], O[None, a:b], l, do[None, a:b],
+                             dQ=dQ[None, a:b], dK=dK[None, a:b], dV=dV[None, a:b], workspace_buf=wsd[b - a][1],
+                             stream=stream)
+
+    out = {"lens": lens, "H": H, "H_kv": Hkv, "D": D}
+    for tag, fn, per_pair in (("packed_fwd", packed_fwd, 4), ("packed_bwd", packed_bwd, 10),
+                              ("per_sequence_fwd", loop_fwd, 4), ("per_sequence_bwd", loop_bwd, 10)):
+        fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(device)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(device)
+        ms = a.elapsed_time(b) / reps
+        out[f"{tag}_ms"] = ms
+        out[f"{tag}_tflops"] = pairs * D * per_pair / (ms * 1e-3) / 1e12
+    dfa.dfa_check_errors(stream)
+    return out
+
+
 # ---------------------------------------------------------------- GPU arm
 def main():
     args = parse()
@@ -483,6 +546,7 @@ def main():
     chunk = None if args.no_chunk_step else chunk_step_timing(w, q, k, v, O, lse, do, stream, dfa)
     local = None if args.window <= 0 else local_window_timing(w, args.window, q, k, v, do, stream, dfa)
     split = None if args.no_split_kv else split_kv_timing(q.device, stream, dfa)
+    varlen = None if args.no_varlen else varlen_timing(q.device, stream, dfa)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -513,6 +577,7 @@ def main():
         "chunk_step": chunk,
         "local_window": local,
         "split_kv": split,
+        "varlen": varlen,
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clk,

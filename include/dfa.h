@@ -177,6 +177,36 @@ dfa_status dfa_attn_bwd_local(const void* q, const void* k, const void* v, const
                               float scale, dfa_sched sched, void* dQ, void* dK, void* dV,
                               void* workspace, size_t ws_bytes, void* stream);
 
+/* Variable-length batch: n_seq sequences of different lengths packed along
+ * the token axis.  The pages (DISTFLASHATTN §3.1-§3.3) define the method for
+ * one sequence per batch entry; a packed batch applies that definition to
+ * every sequence on its own, so no token attends across a sequence boundary
+ * (causal inside each sequence when causal = 1).  One launch covers all
+ * sequences: the work list holds (sequence, head, block) items dealt to the
+ * persistent CTAs, each sequence's causal blocks paired as in BALANCED.
+ *   cu_seqlens: HOST array of n_seq + 1 int32, cu_seqlens[0] = 0, never
+ *               decreasing; sequence s holds tokens [cu[s], cu[s+1]) and
+ *               T = cu[n_seq] is the packed length (empty sequences allowed)
+ *   q, O, dO, dQ: [T, H, D] dense;  k, v, dK, dV: [T, H_kv, D] dense
+ *   lse:        fp32 [H, T] (natural log), saved by the forward for the backward
+ *   workspace:  >= dfa_attn_varlen_workspace_size(...) bytes, 16-byte aligned
+ * bf16 only (DFA_ERR_UNSUPPORTED for fp32), D in {64, 128}.  The work list
+ * and the sequence table are copied from a small ring of pinned host buffers,
+ * so these calls cannot be captured in a CUDA graph.  Backward as
+ * dfa_attn_bwd: from the saved O and lse, never re-running the forward.
+ * Errors: INVALID_ARG for bad offsets, sizes or pointers; WORKSPACE if the
+ * workspace is too small; nothing is launched then. */
+size_t dfa_attn_varlen_workspace_size(const int32_t* cu_seqlens, int n_seq, int H, int H_kv, int D, int bwd);
+dfa_status dfa_attn_fwd_varlen(const void* q, const void* k, const void* v, dfa_dtype dt,
+                               const int32_t* cu_seqlens, int n_seq, int H, int H_kv, int D, int causal,
+                               float scale, void* O, float* lse, void* workspace, size_t ws_bytes,
+                               void* stream);
+dfa_status dfa_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* O,
+                               const float* lse, const void* dO, dfa_dtype dt,
+                               const int32_t* cu_seqlens, int n_seq, int H, int H_kv, int D, int causal,
+                               float scale, void* dQ, void* dK, void* dV, void* workspace,
+                               size_t ws_bytes, void* stream);
+
 /* dfa_attn_fwd for callers that cannot allocate device memory.  The paper
  * has no counterpart to this entry point.  Some callers cannot call
  * cudaMalloc where they run attention: a plugin whose host framework owns
@@ -249,6 +279,16 @@ int dfa_split_piece_tiles(int B, int H, int S, int causal, int n_sms);
  * makespan in (query tile x key tile) units, or -1 on bad arguments. */
 int64_t dfa_build_split_worklist(int n_rows, int n_units, int kv_tiles, int causal, int piece_tiles,
                                  int n_workers, int32_t* offsets, int32_t* items);
+
+/* Work list of a variable-length batch: sequence s has seq_units[s] units
+ * (<= n_units_max) per head, unit u costing u + 1 tiles when causal (the
+ * dfa_build_worklist cost) and seq_units[s] otherwise.  Causal units of one
+ * (sequence, head) are paired with their mirror (cost n_s + 1); pairs and
+ * single units are dealt longest first to the least-loaded worker.  Item
+ * values are (s * heads + h) * n_units_max + u; items needs
+ * n_seq * heads * n_units_max entries at most.  Returns the makespan or -1. */
+int64_t dfa_build_varlen_worklist(int n_seq, const int32_t* seq_units, int heads, int n_units_max,
+                                  int causal, int n_workers, int32_t* offsets, int32_t* items);
 
 /* The pages' distributed schedule at chunk-step granularity (DISTFLASHATTN
  * App. B, Figs. 5-6, and §4.5): P workers own one chunk each, a step computes

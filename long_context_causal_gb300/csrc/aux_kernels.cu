@@ -188,6 +188,81 @@ __global__ void convert_f32_kernel(int64_t n, int H, int S, int D, float scale, 
     }
 }
 
+// Sequence of a packed batch that holds position p, given the non-decreasing
+// starts st[0..n] (st[n] is the end): the last s < n with st[s] <= p.
+__device__ __forceinline__ int seq_of(const int32_t* st, int n, int64_t p) {
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if (st[mid] <= p) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Packed batch: one warp per (padded row p, head h) of the [H, P] arrays;
+// seq = token starts [n+1] then padded starts [n+1].  Rows past a sequence's
+// end are zero.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+bwd_prep_varlen_kernel(int n, int H, int64_t Ttok, int64_t P, int D, const int32_t* __restrict__ seq,
+                       const T* __restrict__ O, const T* __restrict__ dO, const float* __restrict__ lse,
+                       float* __restrict__ lse2, float* __restrict__ delta) {
+    const int64_t row = (int64_t)blockIdx.x * (kThreads / 32) + threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    if (row >= P * H) return;
+    const int h = row % H;
+    const int64_t p = row / H;
+    const int s = seq_of(seq + n + 1, n, p);
+    const int64_t rel = p - seq[n + 1 + s], tok = seq[s] + rel;
+    const int64_t dst = (int64_t)h * P + p;
+    if (rel >= seq[s + 1] - seq[s]) {
+        if (lane == 0) {
+            lse2[dst] = 0.f;
+            delta[dst] = 0.f;
+        }
+        return;
+    }
+    const int64_t src = (tok * H + h) * D;
+    float acc = 0.f;
+    for (int x = lane; x < D / 8; x += 32) {
+        float a[8], c[8];
+        load8<T>(O + src + 8 * x, a);
+        load8<T>(dO + src + 8 * x, c);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc = fmaf(a[e], c[e], acc);
+    }
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) {
+        delta[dst] = acc;
+        lse2[dst] = lse[(int64_t)h * Ttok + tok] * 1.4426950408889634f;
+    }
+}
+
+// Packed batch: dQ [T, H, D] (bf16) = scale * the head-major padded
+// accumulator [H, P, D]; eight head-dim elements per thread.
+__global__ void convert_varlen_bf16_kernel(int n, int H, int64_t Ttok, int64_t P, int D, float scale,
+                                           const int32_t* __restrict__ seq, const float* __restrict__ in,
+                                           __nv_bfloat16* __restrict__ out) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x, n8 = Ttok * H * D / 8;
+    for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < n8; x += stride) {
+        const int64_t o = 8 * x;
+        const int d = (int)(o % D);
+        const int64_t r = o / D;
+        const int h = (int)(r % H);
+        const int64_t tok = r / H;
+        const int s = seq_of(seq, n, tok);
+        const int64_t p = seq[n + 1 + s] + (tok - seq[s]);
+        const float4* src = reinterpret_cast<const float4*>(in + ((int64_t)h * P + p) * D + d);
+        const float4 a = src[0], b = src[1];
+        __nv_bfloat162 v[4] = {__floats2bfloat162_rn(scale * a.x, scale * a.y),
+                               __floats2bfloat162_rn(scale * a.z, scale * a.w),
+                               __floats2bfloat162_rn(scale * b.x, scale * b.y),
+                               __floats2bfloat162_rn(scale * b.z, scale * b.w)};
+        reinterpret_cast<uint4*>(out)[x] = *reinterpret_cast<uint4*>(v);
+    }
+}
+
 dfa_status launched(const char* what) {
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? DFA_OK : fail(DFA_ERR_CUDA, "%s launch: %s", what, cudaGetErrorString(e));
@@ -264,6 +339,27 @@ dfa_status launch_merge_pieces(dfa_dtype dt, int B, int H, int S, int D, int cau
         merge_pieces_kernel<__nv_bfloat16><<<(unsigned)blocks, kThreads, 0, s>>>(
             B, H, S, D, causal, piece_tiles, n_split, O_part, lse_part, (__nv_bfloat16*)O, lse);
     return launched("split-kv merge");
+}
+
+dfa_status launch_bwd_prep_varlen(int n_seq, int H, int64_t T, int64_t P, int D, const int32_t* seq,
+                                  const void* O, const void* dO, const float* lse, float* lse2, float* delta,
+                                  cudaStream_t s) {
+    const int64_t rows = P * H;
+    if (rows == 0 || n_seq <= 0) return DFA_OK;
+    const int64_t blocks = (rows + kThreads / 32 - 1) / (kThreads / 32);
+    bwd_prep_varlen_kernel<__nv_bfloat16><<<(unsigned)blocks, kThreads, 0, s>>>(
+        n_seq, H, T, P, D, seq, (const __nv_bfloat16*)O, (const __nv_bfloat16*)dO, lse, lse2, delta);
+    return launched("varlen bwd prep");
+}
+
+dfa_status launch_convert_varlen(int n_seq, int H, int64_t T, int64_t P, int D, float scale, const int32_t* seq,
+                                 const float* acc, void* out, cudaStream_t s) {
+    const int64_t n8 = T * H * D / 8;
+    if (n8 == 0 || n_seq <= 0) return DFA_OK;
+    const int blocks = 8 * num_sms();
+    convert_varlen_bf16_kernel<<<blocks, kThreads, 0, s>>>(n_seq, H, T, P, D, scale, seq, acc,
+                                                                 (__nv_bfloat16*)out);
+    return launched("varlen dQ convert");
 }
 
 dfa_status launch_delta(dfa_dtype dt, int B, int H, int S, int D, const void* O,

@@ -68,9 +68,11 @@ struct Args {
     float scale, c2;
     const float* lse2;
     const float* delta;
-    float* dq_acc;                // [B, H, S, D] fp32, zeroed by the caller
+    float* dq_acc;                // [B, H, acc_rows, D] fp32, zeroed by the caller
+    int64_t acc_rows;             // Lq; for a packed batch the padded rows per head
     void* dK;                     // [B, Lkv, Hkv, D]
     void* dV;
+    const int32_t* seq;           // packed batch: token starts [B+1], padded starts [B+1]; nullptr: dense
     const int32_t* wl_offsets;
     const int32_t* wl_items;
     int n_units;
@@ -98,13 +100,21 @@ struct Item {
     }
 };
 
+// VARLEN: a packed batch (a.seq set).  The dense kernel is a separate
+// instantiation in which the sequence base is 0 and the lengths are the
+// problem's, so it keeps its registers for the tile loop.
+template <bool VARLEN>
 __device__ __forceinline__ Item decode(const Args& a, int it) {
     Item x;
     const int row = it / a.n_units, unit = it % a.n_units;
     x.b = row / a.Hkv;
     x.g = row % a.Hkv;
-    x.t = a.n_units - 1 - unit;
-    x.n_q = (a.Lq + BT - 1) / BT;
+    int n_k = a.n_units;          // key tiles of the sequence
+    if constexpr (VARLEN) {
+        n_k = (a.seq[x.b + 1] - a.seq[x.b] + BT - 1) / BT;
+    }
+    x.t = n_k - 1 - unit;
+    x.n_q = VARLEN ? n_k : (a.Lq + BT - 1) / BT;
     // first query tile that sees any key of tile t: q_offset + 128 i + 127 >= kv_offset + 128 t
     x.i0 = a.causal ? min(max(x.t + a.rel / BT, 0), x.n_q) : 0;
     x.i1 = x.n_q;
@@ -116,10 +126,23 @@ __device__ __forceinline__ Item decode(const Args& a, int it) {
         x.i1 = i1 < x.i0 ? x.i0 : (int)i1;
     }
     x.ntiles = (a.H / a.Hkv) * (x.i1 - x.i0);
-    x.down = 2 * x.t >= a.n_units;
+    if (VARLEN && x.t < 0) x.ntiles = 0;   // unit past the end of a short sequence
+    x.down = 2 * x.t >= n_k;
     return x;
 }
 
+// Sequence geometry of item x, selected at compile time: the dense kernel
+// reads its lengths from the parameters; the packed-batch kernel re-reads the
+// small, cache-resident sequence table where a value is used instead of
+// holding it in registers across the tile loop (the warps here run at the
+// register limit, and a few more live values cost about a tenth of the speed).
+#define SEQ_LQ(x) (VARLEN ? a.seq[(x).b + 1] - a.seq[(x).b] : a.Lq)
+#define SEQ_LKV(x) (VARLEN ? a.seq[(x).b + 1] - a.seq[(x).b] : a.Lkv)
+#define SEQ_BASE(x) (VARLEN ? a.seq[(x).b] : 0)
+#define SEQ_PBASE(x) (VARLEN ? a.seq[a.B + 1 + (x).b] : 0)
+#define SEQ_TB(x) (VARLEN ? 0 : (x).b)
+
+template <bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO, const Args a) {
@@ -202,29 +225,30 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             return ok;
         };
         for (int it = it_begin; it < it_end && ok; ++it) {
-            const Item x = decode(a, a.wl_items[it]);
+            const Item x = decode<VARLEN>(a, a.wl_items[it]);
             if (x.ntiles == 0) continue;   // key tile entirely above the diagonal: nothing to do
             if (!wait(kv_empty, (kvi & 1) ^ 1)) break;
             ++kv_issued;
             if (lane == 0) {
                 mbar_arrive_expect_tx(kv_full, 2 * kTile);
                 for (int blk = 0; blk < 2; ++blk) {
-                    tma_load_4d(sK + blk * 16384, &tmK, kv_full, blk * 64, x.g, x.t * BT, x.b);
-                    tma_load_4d(sV + blk * 16384, &tmV, kv_full, blk * 64, x.g, x.t * BT, x.b);
+                    tma_load_4d(sK + blk * 16384, &tmK, kv_full, blk * 64, x.g, SEQ_BASE(x) + x.t * BT, SEQ_TB(x));
+                    tma_load_4d(sV + blk * 16384, &tmV, kv_full, blk * 64, x.g, SEQ_BASE(x) + x.t * BT, SEQ_TB(x));
                 }
             }
             __syncwarp();
             for (int k = 0; k < x.ntiles && ok; ++k, ++n) {
                 int h, i;
                 x.tile(k, G, h, i);
-                const size_t side_off = ((size_t)x.b * a.H + h) * a.S_pad + (size_t)i * BT;
+                const size_t side_off = ((size_t)SEQ_TB(x) * a.H + h) * a.S_pad + SEQ_PBASE(x) + (size_t)i * BT;
                 const uint32_t s = n & 1, ph = ((n >> 1) & 1) ^ 1;
                 if (!wait(&q_empty[s], ph)) break;
                 ++q_issued;
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&q_full[s], kTile + kSide);
                     for (int blk = 0; blk < 2; ++blk)
-                        tma_load_4d(sQ + s * kTile + blk * 16384, &tmQ, &q_full[s], blk * 64, h, i * BT, x.b);
+                        tma_load_4d(sQ + s * kTile + blk * 16384, &tmQ, &q_full[s], blk * 64, h, SEQ_BASE(x) + i * BT,
+                                    SEQ_TB(x));
                     bulk_load(sSide + s * kSide, a.lse2 + side_off, 512, &q_full[s]);
                     bulk_load(sSide + s * kSide + 512, a.delta + side_off, 512, &q_full[s]);
                 }
@@ -234,7 +258,8 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&do_full[s], kTile);
                     for (int blk = 0; blk < 2; ++blk)
-                        tma_load_4d(sdO + s * kTile + blk * 16384, &tmdO, &do_full[s], blk * 64, h, i * BT, x.b);
+                        tma_load_4d(sdO + s * kTile + blk * 16384, &tmdO, &do_full[s], blk * 64, h,
+                                    SEQ_BASE(x) + i * BT, SEQ_TB(x));
                 }
                 __syncwarp();
             }
@@ -300,7 +325,7 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             return true;
         };
         for (int it = it_begin; it < it_end && ok; ++it) {
-            const Item x = decode(a, a.wl_items[it]);
+            const Item x = decode<VARLEN>(a, a.wl_items[it]);
             if (x.ntiles == 0) continue;   // key tile entirely above the diagonal: nothing to do
             if (!wait(kv_full, kvi & 1, 0)) break;
             if (!issue_S(n) || !issue_dP(n)) break;
@@ -367,10 +392,10 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             return ok;
         };
         for (int it = it_begin; it < it_end && ok; ++it) {
-            const Item x = decode(a, a.wl_items[it]);
+            const Item x = decode<VARLEN>(a, a.wl_items[it]);
             if (x.ntiles == 0) continue;   // key tile entirely above the diagonal: nothing to do
             const int kvg = x.t * BT + r;
-            const bool row_ok = kvg < a.Lkv;
+            const bool row_ok = kvg < SEQ_LKV(x);
             // local window: this key is seen by queries below q_hi (chunk-relative);
             // q_hi_tile is the lowest such bound over the tile's keys
             const int64_t q_hi = a.win_w > 0 ? ((a.kv_off + kvg) / a.win_c + a.win_w) * a.win_c - a.q_off : INT64_MAX;
@@ -388,9 +413,9 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 const float* dl = lse2 + BT;
                 // Elements outside the causal triangle or the sequence only occur on
                 // the diagonal tile and on ragged edges; elsewhere no mask is applied.
-                const bool full = !(a.causal && i == x.t + a.rel / BT) && (i + 1) * BT <= a.Lq &&
+                const bool full = !(a.causal && i == x.t + a.rel / BT) && (i + 1) * BT <= SEQ_LQ(x) &&
                                   (int64_t)(i + 1) * BT <= q_hi_tile &&
-                                  (x.t + 1) * BT <= a.Lkv;
+                                  (x.t + 1) * BT <= SEQ_LKV(x);
                 // ---- phase 1: P^T = exp2(S^T c - lse2) -> TMEM (bf16) and registers
                 uint32_t u[32], pk[32];
 #pragma unroll
@@ -400,7 +425,7 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
                         for (int z = 0; z < 32; ++z) {
                             const int qg = q0 + c + z;
-                            if (!(row_ok && qg < a.Lq && !(a.causal && kvg + a.rel > qg) && qg < q_hi))
+                            if (!(row_ok && qg < SEQ_LQ(x) && !(a.causal && kvg + a.rel > qg) && qg < q_hi))
                                 u[z] = 0xff800000u;
                         }
                     }
@@ -450,7 +475,7 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             // or fp32 += for a chunk pair's partial gradients); this half's columns
             if (!wait(kd_full, kvi & 1, 1)) break;
             tc_fence_after();
-            const int64_t orow = (((int64_t)x.b * a.Lkv + kvg) * a.Hkv + x.g) * D;
+            const int64_t orow = (((int64_t)SEQ_TB(x) * a.Lkv + SEQ_BASE(x) + kvg) * a.Hkv + x.g) * D;
 #pragma unroll 1
             for (int c = half * 2; c < half * 2 + 2; ++c) {
                 uint32_t uv[32], uk[32];
@@ -509,8 +534,9 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         bool ok = true;
         uint64_t wt = 0;
         for (int it = it_begin; it < it_end && ok; ++it) {
-            const Item x = decode(a, a.wl_items[it]);
+            const Item x = decode<VARLEN>(a, a.wl_items[it]);
             if (x.ntiles == 0) continue;   // key tile entirely above the diagonal: nothing to do
+            const int s_pbase = SEQ_PBASE(x), s_len = SEQ_LQ(x);   // once per item
             for (int k = 0; k < x.ntiles; ++k, ++n) {
                 int h, i;
                 x.tile(k, G, h, i);
@@ -523,9 +549,10 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 // column m with one 16-byte reduction and a warp instruction covers
                 // four full 128-byte rows.
                 const int m = lane & 3;
-                float* base = a.dq_acc + (((int64_t)x.b * a.H + h) * a.Lq + (int64_t)i * BT + m) * D +
+                float* base = a.dq_acc + (((int64_t)SEQ_TB(x) * a.H + h) * (VARLEN ? a.acc_rows : a.Lq) + s_pbase +
+                                          (int64_t)i * BT + m) * D +
                               (warp % 4) * 32 + (lane >> 2) * 4;
-                const int nq = min(BT, a.Lq - i * BT);
+                const int nq = min(BT, s_len - i * BT);
                 // Two halves of 64 query columns (64 registers each); TMEM is
                 // released once the second half has been read.
 #pragma unroll 1
@@ -560,6 +587,12 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     if (threadIdx.x == 0) trace_cta(a.trace, a.trace_cap, t_start, it_end - it_begin);
 }
 
+#undef SEQ_LQ
+#undef SEQ_LKV
+#undef SEQ_BASE
+#undef SEQ_PBASE
+#undef SEQ_TB
+
 }  // namespace
 
 dfa_status tc_bwd_pipelined(const AttnProblem& p, const void* q, const void* k, const void* v, const void* dO,
@@ -570,12 +603,15 @@ dfa_status tc_bwd_pipelined(const AttnProblem& p, const void* q, const void* k, 
     if (rel % BT != 0 || rel > (int64_t)1 << 30 || rel < -((int64_t)1 << 30))
         return fail(DFA_ERR_UNSUPPORTED, "tensor-core backward needs kv_offset - q_offset a multiple of 128");
     alignas(64) CUtensorMap mq, mk, mv, mdo;
-    if (!make_tmap_bshd(&mq, q, p.B, p.Lq, p.H, D, p.q_sb, p.q_ss, p.q_sh) ||
-        !make_tmap_bshd(&mdo, dO, p.B, p.Lq, p.H, D, p.q_sb, p.q_ss, p.q_sh) ||
-        !make_tmap_bshd(&mk, k, p.B, p.Lkv, p.Hkv, D, p.kv_sb, p.kv_ss, p.kv_sh) ||
-        !make_tmap_bshd(&mv, v, p.B, p.Lkv, p.Hkv, D, p.kv_sb, p.kv_ss, p.kv_sh))
+    const int tB = p.seq ? 1 : p.B;   // a packed batch is one tensor row of T tokens
+    if (!make_tmap_bshd(&mq, q, tB, p.Lq, p.H, D, p.q_sb, p.q_ss, p.q_sh) ||
+        !make_tmap_bshd(&mdo, dO, tB, p.Lq, p.H, D, p.q_sb, p.q_ss, p.q_sh) ||
+        !make_tmap_bshd(&mk, k, tB, p.Lkv, p.Hkv, D, p.kv_sb, p.kv_ss, p.kv_sh) ||
+        !make_tmap_bshd(&mv, v, tB, p.Lkv, p.Hkv, D, p.kv_sb, p.kv_ss, p.kv_sh))
         return fail(DFA_ERR_CUDA, "tensor map encoding failed");
     Args a{};
+    a.seq = p.seq;
+    a.acc_rows = p.seq ? S_pad : p.Lq;
     a.B = p.B; a.H = p.H; a.Hkv = p.Hkv; a.Lq = p.Lq; a.Lkv = p.Lkv; a.S_pad = S_pad; a.causal = p.causal;
     a.rel = (int)rel; a.acc_f32 = acc_f32;
     a.q_off = p.q_offset; a.kv_off = p.kv_offset; a.win_c = p.win_c; a.win_w = p.causal ? p.win_w : 0;
@@ -586,9 +622,10 @@ dfa_status tc_bwd_pipelined(const AttnProblem& p, const void* q, const void* k, 
     a.wl_offsets = wl->offsets; a.wl_items = wl->items; a.n_units = wl->n_units;
     a.err = device_error_flag();
     a.trace = cta_trace(&a.trace_cap);
-    if (cudaFuncSetAttribute(bwd_pipe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
+    auto kern = p.seq ? bwd_pipe_kernel<true> : bwd_pipe_kernel<false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
         return fail(DFA_ERR_CUDA, "bwd_pipe: shared memory attribute");
-    bwd_pipe_kernel<<<wl->n_workers, kThreads, kSmem, s>>>(mq, mk, mv, mdo, a);
+    kern<<<wl->n_workers, kThreads, kSmem, s>>>(mq, mk, mv, mdo, a);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? DFA_OK : fail(DFA_ERR_CUDA, "bwd_pipe launch: %s", cudaGetErrorString(e));
 }

@@ -69,9 +69,11 @@ struct BwdArgs {
     float scale, c2;              // c2 = scale * log2(e)
     const float* lse2;            // [B, H, S_pad]  lse * log2(e)
     const float* delta;           // [B, H, S_pad]
-    float* dq_acc;                // [B, H, S, D] fp32, zeroed by the caller
+    float* dq_acc;                // [B, H, acc_rows, D] fp32, zeroed by the caller
+    int64_t acc_rows;             // S; for a packed batch the padded rows per head
     __nv_bfloat16* dK;            // [B, S, Hkv, D]
     __nv_bfloat16* dV;
+    const int32_t* seq;           // packed batch: token starts [B+1], padded starts [B+1]; nullptr: dense
     const int32_t* wl_offsets;
     const int32_t* wl_items;
     int n_units;                  // key tiles per (batch, kv head)
@@ -91,6 +93,7 @@ struct BwdArgs {
 struct BItem {
     int b, g, t, i0, i1, n_q, ntiles;   // query tiles [i0, i1) per head
     bool down;                      // sweep query tiles from the last one down
+    int base, pbase, len;           // packed batch: first token, first padded row, tokens of the sequence
     // k-th tile of the item: head hh of the group (0..G-1), query tile i
     __device__ __forceinline__ void tile(int k, int& hh, int& i) const {
         const int len = i1 - i0, r = k % len;
@@ -99,13 +102,23 @@ struct BItem {
     }
 };
 
+// VARLEN: a packed batch (a.seq set), compiled as its own instantiation so
+// the dense kernel reads its lengths straight from the parameters.
+template <bool VARLEN>
 __device__ __forceinline__ BItem bdecode(const BwdArgs& a, int it) {
     BItem x;
     const int row = it / a.n_units, unit = it % a.n_units;
     x.b = row / a.Hkv;
     x.g = row % a.Hkv;
-    x.t = a.n_units - 1 - unit;          // unit u costs u + 1 query tiles per head
-    x.n_q = (a.S + BT - 1) / BT;
+    int n_k = a.n_units;                 // key tiles of the sequence
+    if constexpr (VARLEN) {
+        x.base = a.seq[x.b];
+        x.pbase = a.seq[a.B + 1 + x.b];
+        x.len = a.seq[x.b + 1] - x.base;
+        n_k = (x.len + BT - 1) / BT;
+    }
+    x.t = n_k - 1 - unit;                // unit u costs u + 1 query tiles per head
+    x.n_q = ((VARLEN ? x.len : a.S) + BT - 1) / BT;
     x.i0 = a.causal ? x.t : 0;
     x.i1 = x.n_q;
     if (a.win_w > 0) {   // local window: queries below q_hi of the tile's last key may see it
@@ -115,11 +128,18 @@ __device__ __forceinline__ BItem bdecode(const BwdArgs& a, int it) {
         x.i1 = i1 < x.i0 ? x.i0 : (int)i1;
     }
     x.ntiles = (a.H / a.Hkv) * (x.i1 - x.i0);
-    x.down = 2 * x.t >= a.n_units;
+    if (VARLEN && x.t < 0) x.ntiles = 0;   // unit past the end of a short sequence
+    x.down = 2 * x.t >= n_k;
     return x;
 }
 
-template <int D>
+// Sequence geometry of item x (see bdecode).
+#define SEQ_LEN(x) (VARLEN ? (x).len : a.S)
+#define SEQ_BASE(x) (VARLEN ? (x).base : 0)
+#define SEQ_PBASE(x) (VARLEN ? (x).pbase : 0)
+#define SEQ_TB(x) (VARLEN ? 0 : (x).b)
+
+template <int D, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -203,14 +223,14 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             return ok;
         };
         for (int it = it_begin; it < it_end && ok; ++it) {
-            const BItem x = bdecode(a, a.wl_items[it]);
+            const BItem x = bdecode<VARLEN>(a, a.wl_items[it]);
             if (!wait(kv_empty, (kvi & 1) ^ 1)) break;
             ++kv_issued;
             if (lane == 0) {
                 mbar_arrive_expect_tx(kv_full, 2 * C::kTile);
                 for (int blk = 0; blk < D / 64; ++blk) {
-                    tma_load_4d(sK + blk * 16384, &tmK, kv_full, blk * 64, x.g, x.t * BT, x.b);
-                    tma_load_4d(sV + blk * 16384, &tmV, kv_full, blk * 64, x.g, x.t * BT, x.b);
+                    tma_load_4d(sK + blk * 16384, &tmK, kv_full, blk * 64, x.g, SEQ_BASE(x) + x.t * BT, SEQ_TB(x));
+                    tma_load_4d(sV + blk * 16384, &tmV, kv_full, blk * 64, x.g, SEQ_BASE(x) + x.t * BT, SEQ_TB(x));
                 }
             }
             __syncwarp();
@@ -218,14 +238,15 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 int hh, i;
                 x.tile(k, hh, i);
                 const int h = x.g * G + hh;
-                const size_t side_off = ((size_t)x.b * a.H + h) * a.S_pad;
+                const size_t side_off = ((size_t)SEQ_TB(x) * a.H + h) * a.S_pad + SEQ_PBASE(x);
                 const uint32_t s = n & 1, ph = ((n >> 1) & 1) ^ 1;
                 if (!wait(&q_empty[s], ph)) break;
                 ++q_issued;
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&q_full[s], C::kTile + kSide);
                     for (int blk = 0; blk < D / 64; ++blk)
-                        tma_load_4d(sQ + s * C::kTile + blk * 16384, &tmQ, &q_full[s], blk * 64, h, i * BT, x.b);
+                        tma_load_4d(sQ + s * C::kTile + blk * 16384, &tmQ, &q_full[s], blk * 64, h, SEQ_BASE(x) + i * BT,
+                                    SEQ_TB(x));
                     bulk_load(sSide + s * kSide, a.lse2 + side_off + i * BT, 512, &q_full[s]);
                     bulk_load(sSide + s * kSide + 512, a.delta + side_off + i * BT, 512, &q_full[s]);
                 }
@@ -235,8 +256,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&do_full[s], C::kTile);
                     for (int blk = 0; blk < D / 64; ++blk)
-                        tma_load_4d(sdO + s * C::kTile + blk * 16384, &tmdO, &do_full[s], blk * 64, h, i * BT,
-                                    x.b);
+                        tma_load_4d(sdO + s * C::kTile + blk * 16384, &tmdO, &do_full[s], blk * 64, h,
+                                    SEQ_BASE(x) + i * BT, SEQ_TB(x));
                 }
                 __syncwarp();
             }
@@ -285,7 +306,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             __syncwarp();
         };
         for (int it = it_begin; it < it_end && ok; ++it) {
-            const BItem x = bdecode(a, a.wl_items[it]);
+            const BItem x = bdecode<VARLEN>(a, a.wl_items[it]);
             if (!wait(kv_full, kvi & 1, 3)) break;
             for (int k = 0; k < x.ntiles; ++k, ++n) {
                 const uint32_t s = n & 1, ph = (n >> 1) & 1;
@@ -366,9 +387,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             return ok;
         };
         for (int it = it_begin; it < it_end && ok; ++it) {
-            const BItem x = bdecode(a, a.wl_items[it]);
+            const BItem x = bdecode<VARLEN>(a, a.wl_items[it]);
             const int kvg = x.t * BT + r;                   // global key index of this thread's row
-            const bool row_ok = kvg < a.S;
+            const bool row_ok = kvg < SEQ_LEN(x);
             const int64_t q_hi = a.win_w > 0 ? ((int64_t)kvg / a.win_c + a.win_w) * a.win_c : INT64_MAX;
             for (int k = 0; k < x.ntiles; ++k, ++n) {
                 int hh, i;
@@ -393,7 +414,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 #pragma unroll
                         for (int z = 0; z < 4; ++z) {
                             const int qg = q0 + c * 32 + e + z;
-                            const bool vis = row_ok && qg < a.S && !(a.causal && kvg > qg) && qg < q_hi;
+                            const bool vis = row_ok && qg < SEQ_LEN(x) && !(a.causal && kvg > qg) && qg < q_hi;
                             const float p = vis ? ex2(fmaf(__uint_as_float(us[e + z]), a.c2, -lv[z])) : 0.f;
                             pp[z] = p;
                             dd[z] = p * (__uint_as_float(ud[e + z]) - dv[z]);
@@ -419,7 +440,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             // ---- epilogue: dV = acc, dK = scale * acc, bf16, [B, S, Hkv, D]
             if (!wait(kd_full, kvi & 1, 1)) break;
             tc_fence_after();
-            const int64_t orow = (((int64_t)x.b * a.S + kvg) * a.Hkv + x.g) * D;
+            const int64_t orow = (((int64_t)SEQ_TB(x) * a.S + SEQ_BASE(x) + kvg) * a.Hkv + x.g) * D;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t uv[32], uk[32];
@@ -463,7 +484,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         bool ok = true;
         uint64_t wt = 0;
         for (int it = it_begin; it < it_end && ok; ++it) {
-            const BItem x = bdecode(a, a.wl_items[it]);
+            const BItem x = bdecode<VARLEN>(a, a.wl_items[it]);
             for (int k = 0; k < x.ntiles; ++k, ++n) {
                 int hh, i;
                 x.tile(k, hh, i);
@@ -483,15 +504,17 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 mbar_arrive(dq_free);
                 if constexpr (D == 128) {
                     // Column c is query row i*128 + c: the warp adds 32 consecutive floats of it.
-                    float* base = a.dq_acc + (((int64_t)x.b * a.H + h) * a.S + (int64_t)i * BT) * D + r;
-                    const int nq = min(BT, a.S - i * BT);
+                    float* base = a.dq_acc + (((int64_t)SEQ_TB(x) * a.H + h) * (VARLEN ? a.acc_rows : a.S) + SEQ_PBASE(x) +
+                                                  (int64_t)i * BT) * D + r;
+                    const int nq = min(BT, SEQ_LEN(x) - i * BT);
 #pragma unroll
                     for (int c = 0; c < BT; ++c)
                         if (c < nq) atomicAdd(base + (int64_t)c * D, __uint_as_float(u[c]));
                 } else {
                     const int qg = i * BT + r;
-                    if (qg < a.S) {
-                        float4* dst = reinterpret_cast<float4*>(a.dq_acc + (((int64_t)x.b * a.H + h) * a.S + qg) * D);
+                    if (qg < SEQ_LEN(x)) {
+                        float4* dst = reinterpret_cast<float4*>(
+                            a.dq_acc + (((int64_t)SEQ_TB(x) * a.H + h) * (VARLEN ? a.acc_rows : a.S) + SEQ_PBASE(x) + qg) * D);
 #pragma unroll
                         for (int e = 0; e < D / 4; ++e)
                             atomicAdd(dst + e, make_float4(__uint_as_float(u[4 * e]), __uint_as_float(u[4 * e + 1]),
@@ -512,17 +535,25 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     if (threadIdx.x == 0) trace_cta(a.trace, a.trace_cap, t_start, it_end - it_begin);
 }
 
+#undef SEQ_LEN
+#undef SEQ_BASE
+#undef SEQ_PBASE
+#undef SEQ_TB
+
 template <int D>
 dfa_status launch(const AttnProblem& p, const void* q, const void* k, const void* v, const void* dO,
                   const float* lse2, const float* delta, int S_pad, float* dq_acc, void* dK, void* dV,
                   const WorkList* wl, cudaStream_t s) {
     alignas(64) CUtensorMap mq, mk, mv, mdo;
-    if (!make_tmap_bshd(&mq, q, p.B, p.Lq, p.H, D, p.q_sb, p.q_ss, p.q_sh) ||
-        !make_tmap_bshd(&mdo, dO, p.B, p.Lq, p.H, D, p.q_sb, p.q_ss, p.q_sh) ||
-        !make_tmap_bshd(&mk, k, p.B, p.Lkv, p.Hkv, D, p.kv_sb, p.kv_ss, p.kv_sh) ||
-        !make_tmap_bshd(&mv, v, p.B, p.Lkv, p.Hkv, D, p.kv_sb, p.kv_ss, p.kv_sh))
+    const int tB = p.seq ? 1 : p.B;   // a packed batch is one tensor row of T tokens
+    if (!make_tmap_bshd(&mq, q, tB, p.Lq, p.H, D, p.q_sb, p.q_ss, p.q_sh) ||
+        !make_tmap_bshd(&mdo, dO, tB, p.Lq, p.H, D, p.q_sb, p.q_ss, p.q_sh) ||
+        !make_tmap_bshd(&mk, k, tB, p.Lkv, p.Hkv, D, p.kv_sb, p.kv_ss, p.kv_sh) ||
+        !make_tmap_bshd(&mv, v, tB, p.Lkv, p.Hkv, D, p.kv_sb, p.kv_ss, p.kv_sh))
         return fail(DFA_ERR_CUDA, "tensor map encoding failed");
     BwdArgs a{};
+    a.seq = p.seq;
+    a.acc_rows = p.seq ? S_pad : p.Lq;
     a.B = p.B; a.H = p.H; a.Hkv = p.Hkv; a.S = p.Lq; a.S_pad = S_pad; a.causal = p.causal;
     a.win_c = p.win_c; a.win_w = p.causal ? p.win_w : 0;
     a.scale = p.scale; a.c2 = p.scale * 1.4426950408889634f;
@@ -532,7 +563,7 @@ dfa_status launch(const AttnProblem& p, const void* q, const void* k, const void
     a.wl_offsets = wl->offsets; a.wl_items = wl->items; a.n_units = wl->n_units;
     a.err = device_error_flag();
     a.trace = cta_trace(&a.trace_cap);
-    auto kern = bwd_tc_kernel<D>;
+    auto kern = p.seq ? bwd_tc_kernel<D, true> : bwd_tc_kernel<D, false>;
     const int smem = BCfg<D>::kSmem;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return fail(DFA_ERR_CUDA, "bwd_tc: shared memory attribute");

@@ -10,6 +10,7 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <string>
 #include <tuple>
 #include <vector>
 
@@ -533,6 +534,208 @@ extern "C" dfa_status dfa_chunk_attn_bwd(const void* q, const void* k, const voi
         return st;
     count_launch(DFA_KERNEL_BWD);
     st = launch_convert(DFA_F32, B, H, Lq, D, scale, dq, dQ_acc, true, s);
+    if (st == DFA_OK) count_launch(DFA_KERNEL_CONVERT);
+    return st;
+}
+
+// ---------------------------------------------------------------- packed (variable-length) batches
+namespace {
+
+// Pinned host buffers for the per-call sequence table and work list of packed
+// batches (these change with every batch, so they are not cached).  A ring of
+// kStages buffers per device, each reused only after the copy that last read
+// it has completed (an event recorded after the copy).
+constexpr int kStages = 4;
+struct Stage {
+    int32_t* host = nullptr;
+    size_t cap = 0;
+    cudaEvent_t ev = nullptr;
+    bool pending = false;
+};
+Stage g_stage[kMaxDevices][kStages];
+int g_stage_next[kMaxDevices] = {};
+std::mutex g_stage_mu;
+
+struct VarlenLayout {
+    size_t delta = 0, lse2 = 0, dq = 0, seq = 0, wl = 0, total = 0;
+    int64_t T = 0, P = 0;        // tokens; 128-row padded rows per head
+    int units_max = 0;           // work units of the longest sequence
+    int64_t items = 0;           // work items over all sequences and heads
+};
+
+// Validates the host offsets; returns false (with a message) on bad input.
+bool varlen_sizes(const int32_t* cu, int n, int unit_rows, int heads, VarlenLayout* L) {
+    if (n < 0) return fail(DFA_ERR_INVALID_ARG, "n_seq must be >= 0"), false;
+    if (!cu) return fail(DFA_ERR_INVALID_ARG, "cu_seqlens is null"), false;
+    if (cu[0] != 0) return fail(DFA_ERR_INVALID_ARG, "cu_seqlens[0] must be 0"), false;
+    int64_t P = 0, items = 0;
+    int umax = 0;
+    for (int s = 0; s < n; ++s) {
+        const int64_t len = (int64_t)cu[s + 1] - cu[s];
+        if (len < 0) return fail(DFA_ERR_INVALID_ARG, "cu_seqlens decreases at %d", s + 1), false;
+        P += (len + 127) / 128 * 128;
+        const int u = (int)((len + unit_rows - 1) / unit_rows);
+        umax = std::max(umax, u);
+        items += (int64_t)u * heads;
+    }
+    if (P > INT32_MAX / 2 || items > INT32_MAX / 2 || (int64_t)n * heads * std::max(umax, 1) > INT32_MAX)
+        return fail(DFA_ERR_INVALID_ARG, "packed batch too large"), false;
+    L->T = cu[n];
+    L->P = P;
+    L->units_max = umax;
+    L->items = items;
+    return true;
+}
+
+bool varlen_layout(const int32_t* cu, int n, int H, int Hkv, int D, bool bwd, VarlenLayout* L) {
+    if (!varlen_sizes(cu, n, bwd ? kBwdUnitRows : kFwdUnitRows, bwd ? Hkv : H, L)) return false;
+    size_t off = 0;
+    if (bwd) {
+        L->delta = off;
+        off = align_up(off + sizeof(float) * (size_t)H * L->P);
+        L->lse2 = off;
+        off = align_up(off + sizeof(float) * (size_t)H * L->P);
+        L->dq = off;
+        off = align_up(off + sizeof(float) * (size_t)H * L->P * D);
+    }
+    // The sequence table and the work list are one contiguous int32 block (one copy).
+    L->seq = off;
+    L->wl = off + sizeof(int32_t) * 2 * ((size_t)n + 1);
+    off = align_up(L->wl + sizeof(int32_t) * (kMaxWorkers + 1 + (size_t)L->items));
+    L->total = off;
+    return true;
+}
+
+// Builds [token starts | padded starts | offsets | items] in a staging buffer
+// and copies it to the workspace on `s`.  Returns the worker count (0 on error).
+int upload_varlen(const int32_t* cu, int n, int unit_rows, int heads, int causal, const VarlenLayout& L,
+                  char* ws, cudaStream_t s) {
+    const int dev = current_device();
+    if (dev < 0) return fail(DFA_ERR_CUDA, "no current device"), 0;
+    const int workers = (int)std::max<int64_t>(1, std::min<int64_t>(num_sms(), L.items));
+    const size_t head = 2 * ((size_t)n + 1), count = head + workers + 1 + (size_t)L.items;
+    std::vector<int32_t> units(n);
+    for (int q = 0; q < n; ++q) units[q] = (cu[q + 1] - cu[q] + unit_rows - 1) / unit_rows;
+    std::lock_guard<std::mutex> lk(g_stage_mu);
+    Stage& st = g_stage[dev][g_stage_next[dev]++ % kStages];
+    if (st.pending) {
+        if (cudaEventSynchronize(st.ev) != cudaSuccess) return fail(DFA_ERR_CUDA, "staging event"), 0;
+        st.pending = false;
+    }
+    if (!st.ev && cudaEventCreateWithFlags(&st.ev, cudaEventDisableTiming) != cudaSuccess)
+        return fail(DFA_ERR_CUDA, "staging event"), 0;
+    if (st.cap < count) {
+        if (st.host) cudaFreeHost(st.host);
+        st.host = nullptr;
+        st.cap = 0;
+        const size_t cap = std::max<size_t>(count, 4096);
+        if (cudaHostAlloc((void**)&st.host, cap * sizeof(int32_t), cudaHostAllocDefault) != cudaSuccess)
+            return fail(DFA_ERR_CUDA, "pinned staging buffer of %zu bytes", cap * sizeof(int32_t)), 0;
+        st.cap = cap;
+    }
+    int32_t* h = st.host;
+    int32_t pad = 0;
+    for (int q = 0; q <= n; ++q) {
+        h[q] = cu[q];
+        h[n + 1 + q] = pad;
+        if (q < n) pad += (cu[q + 1] - cu[q] + 127) / 128 * 128;
+    }
+    if (dfa_build_varlen_worklist(n, units.data(), heads, std::max(L.units_max, 1), causal, workers, h + head,
+                                  h + head + workers + 1) < 0)
+        return fail(DFA_ERR_INVALID_ARG, "could not build the packed-batch work list"), 0;
+    cudaError_t e = cudaMemcpyAsync(ws + L.seq, h, count * sizeof(int32_t), cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return fail(DFA_ERR_CUDA, "packed-batch upload: %s", cudaGetErrorString(e)), 0;
+    if (cudaEventRecord(st.ev, s) != cudaSuccess) return fail(DFA_ERR_CUDA, "staging event record"), 0;
+    st.pending = true;
+    return workers;
+}
+
+AttnProblem varlen_problem(int n, int H, int Hkv, int64_t T, int D, int causal, float scale, const int32_t* seq) {
+    AttnProblem p{};
+    p.B = n; p.H = H; p.Hkv = Hkv; p.Lq = (int)T; p.Lkv = (int)T; p.D = D;
+    p.q_sb = T * H * D; p.q_ss = (int64_t)H * D; p.q_sh = D;
+    p.kv_sb = T * Hkv * D; p.kv_ss = (int64_t)Hkv * D; p.kv_sh = D;
+    p.causal = causal != 0;
+    p.scale = scale;
+    p.seq = seq;
+    return p;
+}
+
+dfa_status varlen_common(dfa_dtype dt, const int32_t* cu, int n, int H, int Hkv, int D, float scale, bool bwd,
+                         void* workspace, size_t ws_bytes, VarlenLayout* L) {
+    dfa_status st;
+    if ((st = check_dtype(dt)) || (st = check_common(1, H, Hkv, D, scale))) return st;
+    if (dt != DFA_BF16) return fail(DFA_ERR_UNSUPPORTED, "packed batches run on the bf16 tensor-core path only");
+    if (!varlen_layout(cu, n, H, Hkv, D, bwd, L)) return DFA_ERR_INVALID_ARG;
+    if (L->T == 0) return DFA_OK;
+    if (!workspace || ws_bytes < L->total)
+        return fail(DFA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", L->total, ws_bytes);
+    if (!aligned16(workspace)) return fail(DFA_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
+    return DFA_OK;
+}
+
+}  // namespace
+
+extern "C" size_t dfa_attn_varlen_workspace_size(const int32_t* cu_seqlens, int n_seq, int H, int H_kv, int D,
+                                                int bwd) {
+    if (H <= 0 || H_kv <= 0 || H % H_kv != 0 || (D != 64 && D != 128)) return 0;
+    VarlenLayout L;
+    const std::string keep = g_msg;   // a size query does not change dfa_last_error()
+    const bool ok = varlen_layout(cu_seqlens, n_seq, H, H_kv, D, bwd != 0, &L);
+    snprintf(g_msg, sizeof(g_msg), "%s", keep.c_str());
+    return ok ? L.total : 0;
+}
+
+extern "C" dfa_status dfa_attn_fwd_varlen(const void* q, const void* k, const void* v, dfa_dtype dt,
+                                          const int32_t* cu_seqlens, int n_seq, int H, int H_kv, int D,
+                                          int causal, float scale, void* O, float* lse, void* workspace,
+                                          size_t ws_bytes, void* stream) {
+    g_msg[0] = 0;
+    VarlenLayout L;
+    dfa_status st = varlen_common(dt, cu_seqlens, n_seq, H, H_kv, D, scale, false, workspace, ws_bytes, &L);
+    if (st || L.T == 0) return st;
+    if ((st = check_ptrs({q, k, v, O, lse}))) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* ws = static_cast<char*>(workspace);
+    const int workers = upload_varlen(cu_seqlens, n_seq, kFwdUnitRows, H, causal, L, ws, s);
+    if (!workers) return DFA_ERR_CUDA;
+    const int32_t* seq = reinterpret_cast<const int32_t*>(ws + L.seq);
+    const int32_t* wl_dev = reinterpret_cast<const int32_t*>(ws + L.wl);
+    const AttnProblem p = varlen_problem(n_seq, H, H_kv, L.T, D, causal, scale, seq);
+    WorkList wl{wl_dev, wl_dev + workers + 1, workers, std::max(L.units_max, 1)};
+    st = tc_fwd(p, q, k, v, O, false, lse, &wl, s);
+    if (st == DFA_OK) count_launch(DFA_KERNEL_FWD);
+    return st;
+}
+
+extern "C" dfa_status dfa_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* O,
+                                          const float* lse, const void* dO, dfa_dtype dt,
+                                          const int32_t* cu_seqlens, int n_seq, int H, int H_kv, int D,
+                                          int causal, float scale, void* dQ, void* dK, void* dV, void* workspace,
+                                          size_t ws_bytes, void* stream) {
+    g_msg[0] = 0;
+    VarlenLayout L;
+    dfa_status st = varlen_common(dt, cu_seqlens, n_seq, H, H_kv, D, scale, true, workspace, ws_bytes, &L);
+    if (st || L.T == 0) return st;
+    if ((st = check_ptrs({q, k, v, O, lse, dO, dQ, dK, dV}))) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* ws = static_cast<char*>(workspace);
+    const int workers = upload_varlen(cu_seqlens, n_seq, kBwdUnitRows, H_kv, causal, L, ws, s);
+    if (!workers) return DFA_ERR_CUDA;
+    const int32_t* seq = reinterpret_cast<const int32_t*>(ws + L.seq);
+    const int32_t* wl_dev = reinterpret_cast<const int32_t*>(ws + L.wl);
+    float* delta = reinterpret_cast<float*>(ws + L.delta);
+    float* lse2 = reinterpret_cast<float*>(ws + L.lse2);
+    float* dq_acc = reinterpret_cast<float*>(ws + L.dq);
+    if ((st = launch_bwd_prep_varlen(n_seq, H, L.T, L.P, D, seq, O, dO, lse, lse2, delta, s))) return st;
+    count_launch(DFA_KERNEL_DELTA);
+    cudaError_t e = cudaMemsetAsync(dq_acc, 0, sizeof(float) * (size_t)H * L.P * D, s);
+    if (e != cudaSuccess) return fail(DFA_ERR_CUDA, "dQ accumulator clear: %s", cudaGetErrorString(e));
+    const AttnProblem p = varlen_problem(n_seq, H, H_kv, L.T, D, causal, scale, seq);
+    WorkList wl{wl_dev, wl_dev + workers + 1, workers, std::max(L.units_max, 1)};
+    if ((st = tc_bwd(p, q, k, v, dO, lse2, delta, (int)L.P, dq_acc, dK, dV, &wl, s))) return st;
+    count_launch(DFA_KERNEL_BWD);
+    st = launch_convert_varlen(n_seq, H, L.T, L.P, D, scale, seq, dq_acc, dQ, s);
     if (st == DFA_OK) count_launch(DFA_KERNEL_CONVERT);
     return st;
 }

@@ -73,6 +73,9 @@ struct FwdArgs {
     // writes its partial to O + s * o_piece_stride, lse + s * lse_piece_stride.
     int n_split, piece_tiles;
     int64_t o_piece_stride, lse_piece_stride;
+    // Variable-length batch: tensors are packed [1, T, heads, D] (Lq = Lkv = T),
+    // lse [1, H, T]; sequence b holds tokens [seq[b], seq[b + 1]).  nullptr: dense.
+    const int32_t* seq;
     int* err;
     uint64_t* trace;              // optional per-CTA timeline (nullptr: off)
     int trace_cap;
@@ -81,6 +84,8 @@ struct FwdArgs {
 struct Item {
     int b, h, g, q0, j0, n_kv;   // key/value tiles [j0, n_kv) can be visible to the block
     int s;                       // key/value piece (0 without split-kv items)
+    int tb, base;                // tensor batch index and first token of the sequence
+    int lq, lkv;                 // query and key/value rows of the sequence
 };
 
 // First key position a query at position qp may see under the local window.
@@ -100,11 +105,23 @@ __device__ __forceinline__ Item decode(const FwdArgs& a, int it, bool win) {
     x.h = row % a.H;
     x.g = x.h / (a.H / a.Hkv);
     x.q0 = unit * kBlockRows;
-    const int total = (a.Lkv + BN - 1) / BN;
-    if (!a.causal) {
+    if (a.seq) {
+        x.tb = 0;
+        x.base = a.seq[x.b];
+        x.lq = x.lkv = a.seq[x.b + 1] - x.base;
+    } else {
+        x.tb = x.b;
+        x.base = 0;
+        x.lq = a.Lq;
+        x.lkv = a.Lkv;
+    }
+    const int total = (x.lkv + BN - 1) / BN;
+    if (x.q0 >= x.lq) {   // past the end of a short sequence: nothing to compute or store
+        x.n_kv = 0;
+    } else if (!a.causal) {
         x.n_kv = total;
     } else {
-        const int64_t last_q = a.q_offset + min(x.q0 + kBlockRows, a.Lq) - 1;
+        const int64_t last_q = a.q_offset + min(x.q0 + kBlockRows, x.lq) - 1;
         const int64_t visible = last_q - a.kv_offset + 1;   // keys [0, visible) may be seen
         const int64_t tiles = (visible + BN - 1) / BN;
         x.n_kv = visible <= 0 ? 0 : (int)(tiles < total ? tiles : total);
@@ -246,7 +263,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 for (int w = 0; w < 2; ++w)
                     for (int blk = 0; blk < D / 64; ++blk)
                         tma_load_4d(sQ + w * C::kTileBytes + blk * 16384, &tmQ, q_full, blk * 64, x.h,
-                                    x.q0 + w * BM, x.b);
+                                    x.base + x.q0 + w * BM, x.tb);
             }
             __syncwarp();
             for (int j = x.j0; j < x.n_kv && ok; ++j) {
@@ -259,7 +276,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                         mbar_arrive_expect_tx(&kv_full[slot], C::kTileBytes);
                         for (int blk = 0; blk < D / 64; ++blk)
                             tma_load_4d(sKV + slot * C::kTileBytes + blk * 16384, which ? &tmV : &tmK,
-                                        &kv_full[slot], blk * 64, x.g, j * BN, x.b);
+                                        &kv_full[slot], blk * 64, x.g, x.base + j * BN, x.tb);
                     }
                     __syncwarp();
                 }
@@ -389,14 +406,14 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 tc_fence_after();
                 // Pass 1: row max over the tile (S read from TMEM 32 columns at a time).
                 const int kv0 = j * BN;
-                const bool edge = kv0 + BN > a.Lkv;
+                const bool edge = kv0 + BN > x.lkv;
                 const bool diag = a.causal && (a.kv_offset + kv0 + BN - 1 > a.q_offset + x.q0 + w * BM);
                 const bool masked = edge || diag || (WIN && kv0 < lo_tile);
                 // Column c of this tile is visible iff lo <= c < lim.
                 int lo = 0, lim = BN;
                 if (masked) {
                     if (WIN && lo_row > kv0) lo = lo_row - kv0 > BN ? BN : (int)(lo_row - kv0);
-                    int64_t v = (int64_t)a.Lkv - kv0;
+                    int64_t v = (int64_t)x.lkv - kv0;
                     if (a.causal) {
                         const int64_t vc = qpos - a.kv_offset - kv0 + 1;
                         v = vc < v ? vc : v;
@@ -438,9 +455,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             }
             if (!ok) break;
             // ---- epilogue: O = O_acc / l, lse = ln(sum exp(s))
-            const bool valid_row = row < a.Lq;
+            const bool valid_row = row < x.lq;
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            const int64_t orow = (((int64_t)x.b * a.Lq + row) * a.H + x.h) * D + x.s * a.o_piece_stride;
+            const int64_t orow = (((int64_t)x.tb * a.Lq + x.base + row) * a.H + x.h) * D + x.s * a.o_piece_stride;
             if (x.n_kv > x.j0) {
                 ok = __all_sync(0xffffffffu, mbar_wait_acc(&o_full[w], qi & 1, abort_flag, a.err, nullptr));
                 if (!ok) break;
@@ -480,7 +497,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 }
             }
             if (valid_row)
-                a.lse[((int64_t)x.b * a.H + x.h) * a.Lq + row + x.s * a.lse_piece_stride] = l > 0.f ? (m_run + __log2f(l)) * kLn2 : -INFINITY;
+                a.lse[((int64_t)x.tb * a.H + x.h) * a.Lq + x.base + row + x.s * a.lse_piece_stride] = l > 0.f ? (m_run + __log2f(l)) * kLn2 : -INFINITY;
         }
         if (threadIdx.x == 128) trace_count(a.trace, a.trace_cap, 5, t);
     }
@@ -536,17 +553,19 @@ static dfa_status launch(const AttnProblem& p, const void* q, const void* k, con
     CUtensorMap mq, mk, mv;
     // With no keys nothing is loaded from K/V; any valid address serves the encoder.
     if (p.Lkv == 0) k = v = q;
-    if (!make_tmap_bshd(&mq, q, p.B, p.Lq, p.H, D, p.q_sb, p.q_ss, p.q_sh) ||
-        !make_tmap_bshd(&mk, k, p.B, p.Lkv, p.Hkv, D, p.kv_sb, p.kv_ss, p.kv_sh) ||
-        !make_tmap_bshd(&mv, v, p.B, p.Lkv, p.Hkv, D, p.kv_sb, p.kv_ss, p.kv_sh))
+    const int tB = p.seq ? 1 : p.B;   // a packed batch is one tensor row of T tokens
+    if (!make_tmap_bshd(&mq, q, tB, p.Lq, p.H, D, p.q_sb, p.q_ss, p.q_sh) ||
+        !make_tmap_bshd(&mk, k, tB, p.Lkv, p.Hkv, D, p.kv_sb, p.kv_ss, p.kv_sh) ||
+        !make_tmap_bshd(&mv, v, tB, p.Lkv, p.Hkv, D, p.kv_sb, p.kv_ss, p.kv_sh))
         return fail(DFA_ERR_CUDA, "tensor map encoding failed");
     FwdArgs a{};
+    a.seq = p.seq;
     a.B = p.B; a.H = p.H; a.Hkv = p.Hkv; a.Lq = p.Lq; a.Lkv = p.Lkv;
     a.q_offset = p.q_offset; a.kv_offset = p.kv_offset; a.causal = p.causal;
     a.win_c = p.win_c; a.win_w = p.causal ? p.win_w : 0;
     a.scale_log2 = p.scale * kLog2e;
     a.O = O; a.lse = lse;
-    a.n_units = (p.Lq + kBlockRows - 1) / kBlockRows;
+    a.n_units = wl ? wl->n_units : (p.Lq + kBlockRows - 1) / kBlockRows;
     a.err = device_error_flag();
     a.trace = cta_trace(&a.trace_cap);
     int grid;

@@ -22,6 +22,11 @@ struct AttnProblem {
     int64_t win_c;                // local window (causal only): chunk length in tokens ...
     int win_w;                    // ... and chunks per window; key kp is visible from query qp iff
                                   // kp <= qp and kp / win_c >= qp / win_c - (win_w - 1).  0: none
+    // Variable-length batch (device, int32): seq[0..B] are the first tokens of
+    // the B sequences in the packed [1, Lq, heads, D] tensors (Lq = Lkv = T
+    // tokens), seq[B+1..2B+1] their first rows in the 128-row-padded per-head
+    // arrays of the backward (lse2, Delta, fp32 dQ accumulator).  nullptr: dense.
+    const int32_t* seq = nullptr;
 };
 
 // Device error flag (set by bounded waits that gave up).  Returns the device
@@ -58,6 +63,14 @@ dfa_status launch_delta(dfa_dtype dt, int B, int H, int S, int D, const void* O,
 // Delta = rowsum(dO * O), both written to [B, H, S_pad] with zero padding.
 dfa_status launch_bwd_prep(dfa_dtype dt, int B, int H, int S, int S_pad, int D, const void* O,
                            const void* dO, const float* lse, float* lse2, float* delta, cudaStream_t s);
+// Packed batch of n_seq sequences, T tokens, bf16 (seq as in AttnProblem::seq,
+// P = padded rows per head): lse2 and Delta [H, P] (zero past each sequence's
+// end) from O, dO [T, H, D] and lse [H, T]; and dQ [T, H, D] = scale * acc [H, P, D].
+dfa_status launch_bwd_prep_varlen(int n_seq, int H, int64_t T, int64_t P, int D, const int32_t* seq,
+                                  const void* O, const void* dO, const float* lse, float* lse2, float* delta,
+                                  cudaStream_t s);
+dfa_status launch_convert_varlen(int n_seq, int H, int64_t T, int64_t P, int D, float scale, const int32_t* seq,
+                                 const float* acc, void* out, cudaStream_t s);
 // out[b, s, h, :] = scale * acc[b, h, s, :] cast to dt (acc is the head-major
 // fp32 dQ accumulator of the tensor-core backward; D a multiple of 8).
 // With accumulate, out is fp32 and the scaled values are added to it.

@@ -137,6 +137,60 @@ extern "C" int64_t dfa_build_split_worklist(int n_rows, int n_units, int kv_tile
     return makespan;
 }
 
+extern "C" int64_t dfa_build_varlen_worklist(int n_seq, const int32_t* seq_units, int heads, int n_units_max,
+                                             int causal, int n_workers, int32_t* offsets, int32_t* items) {
+    if (n_seq < 0 || heads <= 0 || n_units_max < 0 || n_workers <= 0 || !offsets || (n_seq > 0 && !seq_units))
+        return -1;
+    if ((int64_t)n_seq * heads * n_units_max > INT32_MAX) return -1;
+    // Groups dealt as a whole: causal mirror pairs (heavy unit first) of equal
+    // cost n_s + 1, or single units (the middle one, every non-causal unit).
+    struct Group {
+        int64_t cost;
+        int32_t first, second;   // item values; second = -1 for a single unit
+    };
+    std::vector<Group> groups;
+    for (int64_t s = 0; s < n_seq; ++s) {
+        const int64_t n = seq_units[s];
+        if (n < 0 || n > n_units_max) return -1;
+        for (int64_t h = 0; h < heads; ++h) {
+            const int64_t row = (s * heads + h) * n_units_max;
+            if (!causal) {
+                for (int64_t u = 0; u < n; ++u) groups.push_back({n, (int32_t)(row + u), -1});
+                continue;
+            }
+            for (int64_t u = 0; u < (n + 1) / 2; ++u) {
+                const int64_t heavy = n - 1 - u;
+                if (heavy == u) groups.push_back({u + 1, (int32_t)(row + u), -1});
+                else groups.push_back({n + 1, (int32_t)(row + heavy), (int32_t)(row + u)});
+            }
+        }
+    }
+    if (!groups.empty() && !items) return -1;
+    std::stable_sort(groups.begin(), groups.end(), [](const Group& x, const Group& y) { return x.cost > y.cost; });
+    const int64_t W = n_workers;
+    std::vector<std::vector<int32_t>> per(W);
+    using Load = std::pair<int64_t, int64_t>;
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+    for (int64_t w = 0; w < W; ++w) heap.push({0, w});
+    int64_t makespan = 0;
+    for (const Group& g : groups) {
+        Load l = heap.top();
+        heap.pop();
+        per[l.second].push_back(g.first);
+        if (g.second >= 0) per[l.second].push_back(g.second);
+        l.first += g.cost;
+        makespan = std::max(makespan, l.first);
+        heap.push(l);
+    }
+    int64_t pos = 0;
+    for (int64_t w = 0; w < W; ++w) {
+        offsets[w] = (int32_t)pos;
+        for (int32_t it : per[w]) items[pos++] = it;
+    }
+    offsets[W] = (int32_t)pos;
+    return makespan;
+}
+
 extern "C" int dfa_chunk_schedule(int P, dfa_sched sched, int max_steps, int32_t* steps) {
     if (P <= 0 || max_steps <= 0 || !steps) return -1;
     if (sched != DFA_SCHED_BALANCED && sched != DFA_SCHED_UNBALANCED) return -1;

@@ -63,6 +63,11 @@ def _load() -> ctypes.CDLL:
         "dfa_build_worklist": (i64, [i32, i32, i32, i32, p32, p32]),
         "dfa_chunk_schedule": (i32, [i32, i32, i32, p32]),
         "dfa_split_piece_tiles": (i32, [i32, i32, i32, i32, i32]),
+        "dfa_build_varlen_worklist": (i64, [i32, p32, i32, i32, i32, i32, p32, p32]),
+        "dfa_attn_varlen_workspace_size": (sz, [p32, i32, i32, i32, i32, i32]),
+        "dfa_attn_fwd_varlen": (i32, [vp, vp, vp, i32, p32, i32, i32, i32, i32, i32, f32, vp, vp, vp, sz, vp]),
+        "dfa_attn_bwd_varlen": (i32, [vp, vp, vp, vp, vp, vp, i32, p32, i32, i32, i32, i32, i32, f32,
+                                      vp, vp, vp, vp, sz, vp]),
         "dfa_build_split_worklist": (i64, [i32, i32, i32, i32, i32, i32, p32, p32]),
         "dfa_debug_mma": (i32, [i32, vp, vp, vp, vp]),
         "dfa_debug_cta_trace": (i32, [vp, i32]),
@@ -215,6 +220,75 @@ def dfa_attn_fwd(q, k, v, n_chunks: int = 1, causal: bool = True, scale: float |
     return O, lse
 
 
+def _cu_host(cu_seqlens):
+    """Host int32 copy of the sequence offsets (list, numpy array or tensor on any device)."""
+    import numpy as np
+    if isinstance(cu_seqlens, torch.Tensor):
+        cu_seqlens = cu_seqlens.detach().cpu().numpy()
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64).reshape(-1))
+    if cu.size < 1 or np.any(cu < 0) or np.any(cu > 2**31 - 1):
+        raise DfaError(DFA_ERR_INVALID_ARG, "cu_seqlens must hold n_seq + 1 int32 offsets")
+    return cu.astype(np.int32)
+
+
+def _check_packed(cu, T):
+    if int(cu[-1]) != T:
+        raise DfaError(DFA_ERR_INVALID_ARG, f"cu_seqlens ends at {int(cu[-1])}, the packed tensors hold {T} tokens")
+
+
+def _p32(a):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+def dfa_attn_varlen_workspace_size(cu_seqlens, H, H_kv, D, bwd) -> int:
+    cu = _cu_host(cu_seqlens)
+    return int(_lib.dfa_attn_varlen_workspace_size(_p32(cu), cu.size - 1, H, H_kv, D, int(bool(bwd))))
+
+
+def varlen_workspace(cu_seqlens, H, H_kv, D, bwd, device="cuda"):
+    n = dfa_attn_varlen_workspace_size(cu_seqlens, H, H_kv, D, bwd)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+
+
+def dfa_attn_fwd_varlen(q, k, v, cu_seqlens, causal: bool = True, scale: float | None = None, O=None, lse=None,
+                        workspace_buf=None, stream=None):
+    """Packed batch forward: q [T,H,D], k, v [T,H_kv,D]; returns (O [T,H,D], lse fp32 [H,T])."""
+    T, H, D = q.shape
+    Hkv = k.shape[1]
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _dense(t, n)
+    cu = _cu_host(cu_seqlens)
+    _check_packed(cu, T)
+    scale = D ** -0.5 if scale is None else float(scale)
+    O = torch.empty_like(q) if O is None else O
+    lse = torch.empty((H, T), dtype=torch.float32, device=q.device) if lse is None else lse
+    ws = varlen_workspace(cu, H, Hkv, D, False, q.device) if workspace_buf is None else workspace_buf
+    _check(_lib.dfa_attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _dtype(q), _p32(cu), cu.size - 1, H, Hkv, D,
+                                    int(bool(causal)), scale, _ptr(O), _ptr(lse), _ptr(ws), ws.numel(),
+                                    _stream(stream)))
+    return O, lse
+
+
+def dfa_attn_bwd_varlen(q, k, v, O, lse, dO, cu_seqlens, causal: bool = True, scale: float | None = None,
+                        dQ=None, dK=None, dV=None, workspace_buf=None, stream=None):
+    """Packed batch backward from the saved (O, lse): returns (dQ, dK, dV)."""
+    T, H, D = q.shape
+    Hkv = k.shape[1]
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (O, "O"), (lse, "lse"), (dO, "dO")):
+        _dense(t, n)
+    cu = _cu_host(cu_seqlens)
+    _check_packed(cu, T)
+    scale = D ** -0.5 if scale is None else float(scale)
+    dQ = torch.empty_like(q) if dQ is None else dQ
+    dK = torch.empty_like(k) if dK is None else dK
+    dV = torch.empty_like(v) if dV is None else dV
+    ws = varlen_workspace(cu, H, Hkv, D, True, q.device) if workspace_buf is None else workspace_buf
+    _check(_lib.dfa_attn_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(O), _ptr(lse), _ptr(dO), _dtype(q),
+                                    _p32(cu), cu.size - 1, H, Hkv, D, int(bool(causal)), scale,
+                                    _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(ws), ws.numel(), _stream(stream)))
+    return dQ, dK, dV
+
+
 def dfa_attn_fwd_noalloc(q, k, v, O, lse, n_chunks: int = 1, causal: bool = True,
                          scale: float | None = None, sched="balanced", stream=None):
     """dfa_attn_fwd without a workspace: writes the caller's O and lse, allocates nothing."""
@@ -342,6 +416,19 @@ def dfa_build_split_worklist(n_rows: int, n_units: int, kv_tiles: int, causal: b
                                        offsets.ctypes.data_as(p32), items.ctypes.data_as(p32))
     if mk < 0:
         raise DfaError(DFA_ERR_INVALID_ARG, "bad split work-list arguments")
+    return offsets, items[: offsets[-1]], int(mk)
+
+
+def dfa_build_varlen_worklist(seq_units, heads: int, n_units_max: int, causal: bool, n_workers: int):
+    """Host-only: packed-batch items dealt to workers -> (offsets, items, makespan)."""
+    import numpy as np
+    units = np.ascontiguousarray(np.asarray(seq_units, dtype=np.int32).reshape(-1))
+    offsets = np.zeros(n_workers + 1, dtype=np.int32)
+    items = np.zeros(max(units.size * heads * max(n_units_max, 1), 1), dtype=np.int32)
+    mk = _lib.dfa_build_varlen_worklist(units.size, _p32(units), heads, n_units_max, int(bool(causal)), n_workers,
+                                        _p32(offsets), _p32(items))
+    if mk < 0:
+        raise DfaError(DFA_ERR_INVALID_ARG, "bad packed-batch work-list arguments")
     return offsets, items[: offsets[-1]], int(mk)
 
 

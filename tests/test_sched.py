@@ -144,3 +144,38 @@ def test_split_worklist_rejects_bad_arguments():
     for args in [(1, 4, 8, True, 0, 4), (1, 4, 8, True, 4, 0), (-1, 4, 8, True, 4, 4)]:
         with pytest.raises(dfa.DfaError):
             dfa.dfa_build_split_worklist(*args)
+
+
+# ---------------------------------------------------------------- variable-length batches
+@pytest.mark.parametrize("units,heads,causal,W", [([3, 0, 2], 2, True, 4), ([16, 1, 7, 8, 0, 33], 4, True, 152),
+                                                  ([5, 5, 5], 2, False, 6), ([1], 1, True, 1),
+                                                  ([64, 2, 2, 2, 2, 2, 2, 2], 8, True, 148)])
+def test_varlen_worklist_covers_every_unit_once_and_keeps_mirror_pairs(units, heads, causal, W):
+    umax = max(units)
+    offsets, items, makespan = dfa.dfa_build_varlen_worklist(units, heads, umax, causal, W)
+    assert offsets[0] == 0 and np.all(np.diff(offsets) >= 0) and offsets[-1] == len(items)
+    expect = {(s * heads + h) * umax + u for s, n in enumerate(units) for h in range(heads) for u in range(n)}
+    assert sorted(items.tolist()) == sorted(expect)
+    cost = []
+    for w in range(W):
+        mine = items[offsets[w]:offsets[w + 1]].tolist()
+        c = 0
+        for it in mine:
+            row, u = divmod(it, umax)
+            n = units[row // heads]
+            c += (u + 1) if causal else n
+            if causal and u != n - 1 - u:
+                assert (row * umax + (n - 1 - u)) in mine, "a unit travels with its mirror"
+        cost.append(c)
+    assert makespan == max(cost)
+    biggest = max((n + 1) if causal else n for n in units if n) if any(units) else 0
+    assert makespan <= sum(cost) / W + biggest
+
+
+def test_varlen_workspace_and_worklist_reject_bad_offsets():
+    assert dfa.dfa_attn_varlen_workspace_size([0, 100, 50], 4, 2, 128, True) == 0
+    assert dfa.dfa_attn_varlen_workspace_size([1, 100], 4, 2, 128, False) == 0
+    assert dfa.dfa_attn_varlen_workspace_size([0, 100], 4, 3, 128, False) == 0
+    assert dfa.dfa_attn_varlen_workspace_size([0], 4, 2, 128, True) > 0
+    with pytest.raises(dfa.DfaError):
+        dfa.dfa_build_varlen_worklist([3, 5], 2, 4, True, 4)   # a sequence above n_units_max

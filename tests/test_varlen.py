@@ -1,0 +1,114 @@
+"""Variable-length (packed) batches through the C ABI against the fp64 oracle.
+
+Every sequence of a packed batch is plain attention on its own (no token
+attends across a sequence boundary).  Tolerances as in test_parity.py (bf16
+I/O: O 2e-2, lse 1e-3 max abs; each gradient 3e-2 x max|reference gradient|).
+A packed batch holding one sequence, or sequences of one length, computes
+each query block exactly as the dense entry points do, so the forward bits
+and dK/dV bits agree with them; dQ adds its partials with unordered atomics
+and agrees to 2e-2.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from long_context_causal_gb300 import dfa
+from long_context_causal_gb300.inputs import make
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def np64(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def packed(lens, H, Hkv, D, seed, k_scale=1.0):
+    T = int(sum(lens))
+    q, k, v, do = make(1, H, Hkv, T, D, torch.bfloat16, seed=seed, device=DEV, k_scale=k_scale)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    return q[0], k[0], v[0], do[0], cu
+
+
+CASES = [
+    # (lens, H, Hkv, D, causal)
+    ([300, 0, 1000, 1, 129, 2048], 4, 2, 128, True),    # ragged tails, an empty and a one-token sequence
+    ([17, 256, 255, 513], 2, 1, 64, True),               # D = 64 kernels, GQA 2:1
+    ([200, 700], 2, 2, 128, False),                      # non-causal inside each sequence
+    ([128, 128, 384, 4096], 8, 8, 128, True),            # tile-aligned lengths, one long sequence
+]
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_varlen_matches_oracle(case):
+    lens, H, Hkv, D, causal = case
+    q, k, v, do, cu = packed(lens, H, Hkv, D, seed=43)
+    O, lse = dfa.dfa_attn_fwd_varlen(q, k, v, cu, causal=causal)
+    dQ, dK, dV = dfa.dfa_attn_bwd_varlen(q, k, v, O, lse, do, cu, causal=causal)
+    dfa.dfa_check_errors()
+    Or, lr = oracle.attn_fwd_varlen(np64(q), np64(k), np64(v), cu, causal=causal)
+    assert np.max(np.abs(np64(O) - Or)) <= 2e-2, f"{case}: O"
+    assert np.max(np.abs(np64(lse) - lr)) <= 1e-3, f"{case}: lse"
+    ref = oracle.attn_bwd_varlen(np64(q), np64(k), np64(v), np64(do), cu, causal=causal)
+    for name, g, r in zip(("dQ", "dK", "dV"), (dQ, dK, dV), ref):
+        rel = np.max(np.abs(np64(g) - r)) / max(np.max(np.abs(r)), 1e-2)
+        assert rel <= 3e-2, f"{case}: {name} rel err {rel}"
+
+
+def test_one_sequence_is_the_dense_entry_point():
+    q, k, v, do, cu = packed([1536], 4, 2, 128, seed=47)
+    O, lse = dfa.dfa_attn_fwd_varlen(q, k, v, cu)
+    g = dfa.dfa_attn_bwd_varlen(q, k, v, O, lse, do, cu)
+    Od, ld = dfa.dfa_attn_fwd(q[None], k[None], v[None])
+    gd = dfa.dfa_attn_bwd(q[None], k[None], v[None], Od, ld, do[None])
+    dfa.dfa_check_errors()
+    assert torch.equal(O, Od[0]) and torch.equal(lse, ld[0])
+    assert torch.equal(g[1], gd[1][0]) and torch.equal(g[2], gd[2][0])
+    assert torch.max(torch.abs(g[0].float() - gd[0][0].float())).item() <= 2e-2
+
+
+def test_equal_lengths_are_the_dense_batch():
+    n, L, H, Hkv, D = 3, 640, 2, 2, 64
+    q, k, v, do, cu = packed([L] * n, H, Hkv, D, seed=53)
+    O, lse = dfa.dfa_attn_fwd_varlen(q, k, v, cu)
+    Od, ld = dfa.dfa_attn_fwd(q.view(n, L, H, D), k.view(n, L, Hkv, D), v.view(n, L, Hkv, D))
+    torch.cuda.synchronize()
+    assert torch.equal(O.view(n, L, H, D), Od)
+    assert torch.equal(lse.view(H, n, L).transpose(0, 1), ld)
+
+
+def test_many_short_sequences_in_one_launch():
+    rng = np.random.default_rng(59)
+    lens = rng.integers(1, 700, 40).tolist()
+    q, k, v, do, cu = packed(lens, 4, 1, 128, seed=61, k_scale=2.0)
+    launches = dfa.dfa_launch_count("fwd")
+    O, lse = dfa.dfa_attn_fwd_varlen(q, k, v, cu)
+    dQ, dK, dV = dfa.dfa_attn_bwd_varlen(q, k, v, O, lse, do, cu)
+    dfa.dfa_check_errors()
+    assert dfa.dfa_launch_count("fwd") == launches + 1
+    Or, lr = oracle.attn_fwd_varlen(np64(q), np64(k), np64(v), cu)
+    assert np.max(np.abs(np64(O) - Or)) <= 2e-2
+    assert np.max(np.abs(np64(lse) - lr)) <= 1e-3
+    ref = oracle.attn_bwd_varlen(np64(q), np64(k), np64(v), np64(do), cu)
+    for name, g, r in zip(("dQ", "dK", "dV"), (dQ, dK, dV), ref):
+        rel = np.max(np.abs(np64(g) - r)) / max(np.max(np.abs(r)), 1e-2)
+        assert rel <= 3e-2, f"{name} rel err {rel}"
+
+
+def test_empty_batch_and_bad_offsets():
+    q, k, v, do, cu = packed([64], 2, 2, 128, seed=67)
+    O, lse = dfa.dfa_attn_fwd_varlen(q[:0], k[:0], v[:0], [0])
+    assert O.shape == (0, 2, 128)
+    with pytest.raises(dfa.DfaError) as e:
+        dfa.dfa_attn_fwd_varlen(q, k, v, cu, workspace_buf=torch.empty(16, dtype=torch.uint8, device=DEV))
+    assert e.value.status == dfa.DFA_ERR_WORKSPACE
+    with pytest.raises(dfa.DfaError) as e:   # offsets that end past the packed tensor
+        dfa.dfa_attn_fwd_varlen(q, k, v, [0, 100])
+    assert e.value.status == dfa.DFA_ERR_INVALID_ARG
+    with pytest.raises(dfa.DfaError) as e:
+        dfa.dfa_attn_fwd_varlen(q, k, v, [0, 40, 20])
+    assert e.value.status == dfa.DFA_ERR_INVALID_ARG
+    with pytest.raises(dfa.DfaError) as e:
+        dfa.dfa_attn_fwd_varlen(q.float(), k.float(), v.float(), cu)
+    assert e.value.status == dfa.DFA_ERR_UNSUPPORTED
