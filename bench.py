@@ -324,40 +324,50 @@ def local_window_timing(w, window, q, k, v, do, stream, dfa, reps=3):
     return out
 
 
-SPLIT_KV_SHAPES = [(1, 1, 1, 32768, 128), (1, 4, 4, 8192, 128)]
+SPLIT_KV_SHAPES = [(1, 1, 1, 32768, 128), (1, 1, 1, 16384, 128)]
 
 
 def split_kv_timing(device, stream, dfa, reps=10):
-    """Causal forward of problems with fewer 256-row query blocks than SMs, with the
-    plain balanced list and with split-kv helper items (pieces of each block's
-    key range computed by other CTAs, then merged).  Inputs of these sizes stay
-    in L2; the forward is compute-bound either way.  Reported beside the headline."""
+    """Causal forward and backward of problems with fewer 256-row query blocks
+    (forward) or key-tile pairs (backward) than SMs, with the plain balanced
+    list and with split-kv helper items (pieces of each block's key range, or
+    of each key tile's query range, computed by other CTAs, then merged or
+    added).  Inputs of these sizes stay in L2; both passes are compute-bound
+    either way.  Reported beside the headline."""
     import torch
     from long_context_causal_gb300.inputs import make
     out = []
     for B, H, Hkv, S, D in SPLIT_KV_SHAPES:
-        q, k, v, _ = make(B, H, Hkv, S, D, torch.bfloat16, seed=3, device=device)
+        q, k, v, do = make(B, H, Hkv, S, D, torch.bfloat16, seed=3, device=device)
         O = torch.empty_like(q)
         lse = torch.empty((B, H, S), dtype=torch.float32, device=device)
-        ws = dfa.workspace(B, H, Hkv, S, D, 1, False, device)
-        flops = B * H * S * (S + 1) // 2 * D * 4
+        dQ, dK, dV = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        wsf = dfa.workspace(B, H, Hkv, S, D, 1, False, device)
+        wsb = dfa.workspace(B, H, Hkv, S, D, 1, True, device)
+        pairs = B * H * S * (S + 1) // 2 * D
         row = {"B": B, "H": H, "H_kv": Hkv, "S": S, "D": D}
         for sched in ("balanced", "split_kv"):
             def fwd():
-                dfa.dfa_attn_fwd(q, k, v, sched=sched, O=O, lse=lse, workspace_buf=ws, stream=stream)
-            for _ in range(3):
-                fwd()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            torch.cuda.synchronize(device)
-            a.record(stream)
-            for _ in range(reps):
-                fwd()
-            b.record(stream)
-            torch.cuda.synchronize(device)
-            ms = a.elapsed_time(b) / reps
-            row[f"{sched}_fwd_ms"] = ms
-            row[f"{sched}_fwd_tflops"] = flops / (ms * 1e-3) / 1e12
-        row["speedup"] = row["balanced_fwd_ms"] / row["split_kv_fwd_ms"]
+                dfa.dfa_attn_fwd(q, k, v, sched=sched, O=O, lse=lse, workspace_buf=wsf, stream=stream)
+
+            def bwd():
+                dfa.dfa_attn_bwd(q, k, v, O, lse, do, sched=sched, dQ=dQ, dK=dK, dV=dV, workspace_buf=wsb,
+                                 stream=stream)
+            for tag, fn, per_pair in (("fwd", fwd, 4), ("bwd", bwd, 10)):
+                for _ in range(3):
+                    fn()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize(device)
+                e0.record(stream)
+                for _ in range(reps):
+                    fn()
+                e1.record(stream)
+                torch.cuda.synchronize(device)
+                ms = e0.elapsed_time(e1) / reps
+                row[f"{sched}_{tag}_ms"] = ms
+                row[f"{sched}_{tag}_tflops"] = pairs * per_pair / (ms * 1e-3) / 1e12
+        row["fwd_speedup"] = row["balanced_fwd_ms"] / row["split_kv_fwd_ms"]
+        row["bwd_speedup"] = row["balanced_bwd_ms"] / row["split_kv_bwd_ms"]
         out.append(row)
     dfa.dfa_check_errors(stream)
     return out

@@ -67,8 +67,13 @@ typedef enum { DFA_F32 = 0, DFA_BF16 = 1 } dfa_dtype;
  *   key/value range is cut into pieces of dfa_split_piece_tiles() 128-key
  *   tiles; each piece is an item of its own whose fp32 partial (O, lse) goes
  *   to the workspace, and a merge kernel combines each row's pieces with the
- *   rescale-and-merge rule.  Larger problems, the local window, fp32 I/O, the
- *   no-alloc forward and every backward treat it as BALANCED. */
+ *   rescale-and-merge rule.  In a bf16 head-dim-128 backward whose mirror
+ *   pairs of key tiles number at most 3/4 of the SMs, every key tile's query range is cut
+ *   into pieces of dfa_split_bwd_piece_tiles() query tiles, and each piece
+ *   adds its partial dK, dV to fp32 accumulators in the workspace (vector
+ *   reductions), cast to bf16 at the end.  Larger problems, the local
+ *   window, fp32 I/O, head dim 64 and the no-alloc forward treat it as
+ *   BALANCED. */
 typedef enum { DFA_SCHED_BALANCED = 0, DFA_SCHED_UNBALANCED = 1, DFA_SCHED_SPLIT_KV = 2 } dfa_sched;
 
 /* One chunk step (DISTFLASHATTN App. D: a worker's step advances its attention
@@ -279,6 +284,25 @@ int dfa_split_piece_tiles(int B, int H, int S, int causal, int n_sms);
  * makespan in (query tile x key tile) units, or -1 on bad arguments. */
 int64_t dfa_build_split_worklist(int n_rows, int n_units, int kv_tiles, int causal, int piece_tiles,
                                  int n_workers, int32_t* offsets, int32_t* items);
+
+/* Split-kv for the backward (SPLIT_KV): query-tile piece length for a bf16
+ * head-dim-128 backward of B * H_kv key-tile rows of S tokens on n_sms SMs,
+ * or 0 when the mirror pairs of key tiles number more than 3/4 of n_sms (or
+ * nothing gains).  Pieces hold at least 16 query tiles and number about
+ * twice n_sms. */
+int dfa_split_bwd_piece_tiles(int B, int H_kv, int S, int causal, int n_sms);
+
+/* Work list of backward split-kv items.  Unit u of a row is key tile
+ * t = kv_tiles - 1 - u, which sees query tiles [t, kv_tiles) when causal and
+ * all of them otherwise; that range is cut into pieces of piece_tiles tiles
+ * [t + s * piece_tiles, ...) and every non-empty piece is an item with value
+ * (row * kv_tiles + u) * n_split + s, n_split = ceil(kv_tiles / piece_tiles).
+ * Each piece adds its partial dK, dV (fp32) to accumulators shared with the
+ * other pieces of its key tile (DISTFLASHATTN §3.3: a helper computes part of
+ * a worker's gradients and hands them back).  Dealt longest first to the
+ * least-loaded worker.  Returns the makespan in query tiles, or -1. */
+int64_t dfa_build_bwd_split_worklist(int n_rows, int kv_tiles, int causal, int piece_tiles, int n_workers,
+                                     int32_t* offsets, int32_t* items);
 
 /* Work list of a variable-length batch: sequence s has seq_units[s] units
  * (<= n_units_max) per head, unit u costing u + 1 tiles when causal (the

@@ -263,6 +263,17 @@ __global__ void convert_varlen_bf16_kernel(int n, int H, int64_t Ttok, int64_t P
     }
 }
 
+// fp32 -> bf16, eight elements per thread (n a multiple of 8).
+__global__ void cast_bf16_kernel(int64_t n, const float* __restrict__ in, __nv_bfloat16* __restrict__ out) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < n / 8; x += stride) {
+        const float4 a = reinterpret_cast<const float4*>(in)[2 * x], b = reinterpret_cast<const float4*>(in)[2 * x + 1];
+        __nv_bfloat162 r[4] = {__floats2bfloat162_rn(a.x, a.y), __floats2bfloat162_rn(a.z, a.w),
+                               __floats2bfloat162_rn(b.x, b.y), __floats2bfloat162_rn(b.z, b.w)};
+        reinterpret_cast<uint4*>(out)[x] = *reinterpret_cast<uint4*>(r);
+    }
+}
+
 dfa_status launched(const char* what) {
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? DFA_OK : fail(DFA_ERR_CUDA, "%s launch: %s", what, cudaGetErrorString(e));
@@ -360,6 +371,13 @@ dfa_status launch_convert_varlen(int n_seq, int H, int64_t T, int64_t P, int D, 
     convert_varlen_bf16_kernel<<<blocks, kThreads, 0, s>>>(n_seq, H, T, P, D, scale, seq, acc,
                                                                  (__nv_bfloat16*)out);
     return launched("varlen dQ convert");
+}
+
+dfa_status launch_cast_bf16(int64_t n, const float* in, void* out, cudaStream_t s) {
+    if (n == 0) return DFA_OK;
+    if (n % 8 != 0) return fail(DFA_ERR_INVALID_ARG, "cast: element count not a multiple of 8");
+    cast_bf16_kernel<<<8 * num_sms(), kThreads, 0, s>>>(n, in, static_cast<__nv_bfloat16*>(out));
+    return launched("bf16 cast");
 }
 
 dfa_status launch_delta(dfa_dtype dt, int B, int H, int S, int D, const void* O,

@@ -76,6 +76,7 @@ struct Args {
     const int32_t* wl_offsets;
     const int32_t* wl_items;
     int n_units;
+    int n_split, piece_tiles;     // split-kv pieces of each key tile's query range (SPLIT)
     int* err;
     uint64_t* trace;
     int trace_cap;
@@ -100,12 +101,19 @@ struct Item {
     }
 };
 
-// VARLEN: a packed batch (a.seq set).  The dense kernel is a separate
-// instantiation in which the sequence base is 0 and the lengths are the
-// problem's, so it keeps its registers for the tile loop.
-template <bool VARLEN>
+// VARLEN: a packed batch (a.seq set).  SPLIT: split-kv items, a piece of
+// piece_tiles query tiles of a key tile's range (item value * n_split + piece);
+// their dK/dV go to fp32 accumulators by reduction.  The dense kernel is a
+// separate instantiation in which the sequence base is 0 and the lengths are
+// the problem's, so it keeps its registers for the tile loop.
+template <bool VARLEN, bool SPLIT>
 __device__ __forceinline__ Item decode(const Args& a, int it) {
     Item x;
+    int piece = 0;
+    if constexpr (SPLIT) {
+        piece = it % a.n_split;
+        it /= a.n_split;
+    }
     const int row = it / a.n_units, unit = it % a.n_units;
     x.b = row / a.Hkv;
     x.g = row % a.Hkv;
@@ -125,6 +133,11 @@ __device__ __forceinline__ Item decode(const Args& a, int it) {
         if (i1 > x.n_q) i1 = x.n_q;
         x.i1 = i1 < x.i0 ? x.i0 : (int)i1;
     }
+    if constexpr (SPLIT) {   // this piece's query tiles only
+        const int lo = x.i0 + piece * a.piece_tiles;
+        x.i1 = min(x.i1, lo + a.piece_tiles);
+        x.i0 = min(lo, x.i1);
+    }
     x.ntiles = (a.H / a.Hkv) * (x.i1 - x.i0);
     if (VARLEN && x.t < 0) x.ntiles = 0;   // unit past the end of a short sequence
     x.down = 2 * x.t >= n_k;
@@ -142,7 +155,7 @@ __device__ __forceinline__ Item decode(const Args& a, int it) {
 #define SEQ_PBASE(x) (VARLEN ? a.seq[a.B + 1 + (x).b] : 0)
 #define SEQ_TB(x) (VARLEN ? 0 : (x).b)
 
-template <bool VARLEN>
+template <bool VARLEN, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO, const Args a) {
@@ -225,7 +238,7 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             return ok;
         };
         for (int it = it_begin; it < it_end && ok; ++it) {
-            const Item x = decode<VARLEN>(a, a.wl_items[it]);
+            const Item x = decode<VARLEN, SPLIT>(a, a.wl_items[it]);
             if (x.ntiles == 0) continue;   // key tile entirely above the diagonal: nothing to do
             if (!wait(kv_empty, (kvi & 1) ^ 1)) break;
             ++kv_issued;
@@ -325,7 +338,7 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             return true;
         };
         for (int it = it_begin; it < it_end && ok; ++it) {
-            const Item x = decode<VARLEN>(a, a.wl_items[it]);
+            const Item x = decode<VARLEN, SPLIT>(a, a.wl_items[it]);
             if (x.ntiles == 0) continue;   // key tile entirely above the diagonal: nothing to do
             if (!wait(kv_full, kvi & 1, 0)) break;
             if (!issue_S(n) || !issue_dP(n)) break;
@@ -392,7 +405,7 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             return ok;
         };
         for (int it = it_begin; it < it_end && ok; ++it) {
-            const Item x = decode<VARLEN>(a, a.wl_items[it]);
+            const Item x = decode<VARLEN, SPLIT>(a, a.wl_items[it]);
             if (x.ntiles == 0) continue;   // key tile entirely above the diagonal: nothing to do
             const int kvg = x.t * BT + r;
             const bool row_ok = kvg < SEQ_LKV(x);
@@ -480,7 +493,20 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             for (int c = half * 2; c < half * 2 + 2; ++c) {
                 uint32_t uv[32], uk[32];
                 tmem_ld32x2(tmem + lane_base + kColDV + c * 32, tmem + lane_base + kColDK + c * 32, uv, uk);
-                if (row_ok && a.acc_f32) {
+                if constexpr (SPLIT) {   // a piece's partial: fp32 reductions, other pieces add to the same rows
+                    if (row_ok) {
+                        float* pv = static_cast<float*>(a.dV) + orow + c * 32;
+                        float* pkk = static_cast<float*>(a.dK) + orow + c * 32;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            red_add_v4(pv + 4 * e, __uint_as_float(uv[4 * e]), __uint_as_float(uv[4 * e + 1]),
+                                       __uint_as_float(uv[4 * e + 2]), __uint_as_float(uv[4 * e + 3]));
+                            red_add_v4(pkk + 4 * e, a.scale * __uint_as_float(uk[4 * e]),
+                                       a.scale * __uint_as_float(uk[4 * e + 1]), a.scale * __uint_as_float(uk[4 * e + 2]),
+                                       a.scale * __uint_as_float(uk[4 * e + 3]));
+                        }
+                    }
+                } else if (row_ok && a.acc_f32) {
                     float4* pv = reinterpret_cast<float4*>(static_cast<float*>(a.dV) + orow + c * 32);
                     float4* pkk = reinterpret_cast<float4*>(static_cast<float*>(a.dK) + orow + c * 32);
 #pragma unroll
@@ -534,7 +560,7 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         bool ok = true;
         uint64_t wt = 0;
         for (int it = it_begin; it < it_end && ok; ++it) {
-            const Item x = decode<VARLEN>(a, a.wl_items[it]);
+            const Item x = decode<VARLEN, SPLIT>(a, a.wl_items[it]);
             if (x.ntiles == 0) continue;   // key tile entirely above the diagonal: nothing to do
             const int s_pbase = SEQ_PBASE(x), s_len = SEQ_LQ(x);   // once per item
             for (int k = 0; k < x.ntiles; ++k, ++n) {
@@ -622,7 +648,12 @@ dfa_status tc_bwd_pipelined(const AttnProblem& p, const void* q, const void* k, 
     a.wl_offsets = wl->offsets; a.wl_items = wl->items; a.n_units = wl->n_units;
     a.err = device_error_flag();
     a.trace = cta_trace(&a.trace_cap);
-    auto kern = p.seq ? bwd_pipe_kernel<true> : bwd_pipe_kernel<false>;
+    const bool split = wl->n_split > 1;
+    if (split && (!acc_f32 || p.seq || wl->piece_tiles <= 0))
+        return fail(DFA_ERR_INVALID_ARG, "split-kv backward pieces need fp32 dK/dV accumulators");
+    a.n_split = wl->n_split;
+    a.piece_tiles = wl->piece_tiles;
+    auto kern = p.seq ? bwd_pipe_kernel<true, false> : split ? bwd_pipe_kernel<false, true> : bwd_pipe_kernel<false, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
         return fail(DFA_ERR_CUDA, "bwd_pipe: shared memory attribute");
     kern<<<wl->n_workers, kThreads, kSmem, s>>>(mq, mk, mv, mdo, a);

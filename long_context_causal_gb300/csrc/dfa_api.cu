@@ -105,10 +105,39 @@ const CachedList* get_split_list(int rows, int units, int kv_tiles, int causal, 
     return &(g_split_lists[key] = c);
 }
 
+// Backward split-kv pieces (dfa_build_bwd_split_worklist); key (rows,
+// kv_tiles, causal, piece_tiles, workers).
+std::map<std::tuple<int, int, int, int, int>, CachedList> g_bwd_split_lists;
+
+int64_t count_bwd_pieces(int rows, int kv_tiles, int causal, int piece) {
+    int64_t n = 0;
+    for (int t = 0; t < kv_tiles; ++t) n += ((causal ? kv_tiles - t : kv_tiles) + piece - 1) / piece;
+    return n * rows;
+}
+
+const CachedList* get_bwd_split_list(int rows, int kv_tiles, int causal, int piece, int workers) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto key = std::make_tuple(rows, kv_tiles, causal, piece, workers);
+    auto it = g_bwd_split_lists.find(key);
+    if (it != g_bwd_split_lists.end()) return &it->second;
+    const int64_t n = count_bwd_pieces(rows, kv_tiles, causal, piece);
+    CachedList c;
+    c.count = (size_t)workers + 1 + (size_t)n;
+    c.workers = workers;
+    if (cudaHostAlloc((void**)&c.host, c.count * sizeof(int32_t), cudaHostAllocDefault) != cudaSuccess)
+        return nullptr;
+    if (dfa_build_bwd_split_worklist(rows, kv_tiles, causal, piece, workers, c.host, c.host + workers + 1) < 0 ||
+        c.host[workers] != n) {
+        cudaFreeHost(c.host);
+        return nullptr;
+    }
+    return &(g_bwd_split_lists[key] = c);
+}
+
 struct Layout {
-    size_t delta = 0, lse2 = 0, dq = 0, wl = 0, opart = 0, lpart = 0, total = 0;
+    size_t delta = 0, lse2 = 0, dq = 0, wl = 0, opart = 0, lpart = 0, dk = 0, dv = 0, total = 0;
     int S_pad = 0;
-    int n_split = 1;   // forward: split-kv pieces the workspace has room for
+    int n_split = 1;   // split-kv pieces the workspace has room for
 };
 
 Layout layout(int B, int H, int Hkv, int S, int D, bool bwd) {
@@ -127,13 +156,18 @@ Layout layout(int B, int H, int Hkv, int S, int D, bool bwd) {
     const size_t units = bwd ? (size_t)(S + kBwdUnitRows - 1) / kBwdUnitRows
                              : (size_t)(S + kFwdUnitRows - 1) / kFwdUnitRows;
     const size_t rows = bwd ? (size_t)B * Hkv : (size_t)B * H;
-    if (!bwd) {
-        // Room for SPLIT_KV pieces when the problem is small enough to be split;
-        // the causal plan has the shortest pieces, so it bounds both masks.
-        const int piece = dfa_split_piece_tiles(B, H, S, 1, num_sms());
-        if (piece > 0) L.n_split = (int)(((S + 127) / 128 + piece - 1) / piece);
-    }
+    // Room for SPLIT_KV pieces when the problem is small enough to be split;
+    // the causal plan has the shortest pieces, so it bounds both masks.
+    const int piece = bwd ? (D == 128 ? dfa_split_bwd_piece_tiles(B, Hkv, S, 1, num_sms()) : 0)
+                          : dfa_split_piece_tiles(B, H, S, 1, num_sms());
+    if (piece > 0) L.n_split = (int)(((S + 127) / 128 + piece - 1) / piece);
     off = align_up(off + sizeof(int32_t) * (kMaxWorkers + 1 + rows * units * (size_t)L.n_split));
+    if (bwd && L.n_split > 1) {   // fp32 dK, dV accumulators [B, S, H_kv, D] the pieces add into
+        L.dk = off;
+        off = align_up(off + sizeof(float) * (size_t)B * S * Hkv * D);
+        L.dv = off;
+        off = align_up(off + sizeof(float) * (size_t)B * S * Hkv * D);
+    }
     if (L.n_split > 1) {
         L.opart = off;
         off = align_up(off + sizeof(float) * (size_t)L.n_split * B * S * H * D);
@@ -425,6 +459,38 @@ static dfa_status attn_bwd_impl(const void* q, const void* k, const void* v, con
     cudaError_t e = cudaMemsetAsync(dq_acc, 0, sizeof(float) * (size_t)B * S * H * D, s);
     if (e != cudaSuccess) return fail(DFA_ERR_CUDA, "dQ accumulator clear: %s", cudaGetErrorString(e));
     const int units = (S + kBwdUnitRows - 1) / kBwdUnitRows;
+    const int piece = sched == DFA_SCHED_SPLIT_KV && D == 128 && !window
+                          ? dfa_split_bwd_piece_tiles(B, H_kv, S, causal, num_sms()) : 0;
+    if (piece > 0) {
+        // Helper items: pieces of every key tile's query range, each adding its
+        // partial dK, dV to fp32 accumulators; then the bf16 casts.
+        const int n_split = (units + piece - 1) / piece;
+        if (n_split > L.n_split) return fail(DFA_ERR_WORKSPACE, "split-kv plan exceeds the workspace layout");
+        const int64_t np = count_bwd_pieces(B * H_kv, units, causal != 0, piece);
+        const int workers = (int)std::min<int64_t>(num_sms(), np);
+        const CachedList* c = get_bwd_split_list(B * H_kv, units, causal != 0, piece, workers);
+        if (!c) return fail(DFA_ERR_CUDA, "could not build the split-kv work list");
+        int32_t* dev = reinterpret_cast<int32_t*>(ws + L.wl);
+        if ((st = upload_list(c, dev, s))) return st;
+        WorkList wl{dev, dev + workers + 1, workers, units};
+        wl.n_split = n_split;
+        wl.piece_tiles = piece;
+        float* dk_acc = reinterpret_cast<float*>(ws + L.dk);
+        float* dv_acc = reinterpret_cast<float*>(ws + L.dv);
+        const size_t kv_elems = (size_t)B * S * H_kv * D;
+        if ((e = cudaMemsetAsync(dk_acc, 0, sizeof(float) * kv_elems, s)) != cudaSuccess ||
+            (e = cudaMemsetAsync(dv_acc, 0, sizeof(float) * kv_elems, s)) != cudaSuccess)
+            return fail(DFA_ERR_CUDA, "dK/dV accumulator clear: %s", cudaGetErrorString(e));
+        if ((st = tc_bwd_pipelined(p, q, k, v, dO, lse2, delta, L.S_pad, dq_acc, dk_acc, dv_acc, true, &wl, s)))
+            return st;
+        count_launch(DFA_KERNEL_BWD);
+        if ((st = launch_convert(dt, B, H, S, D, scale, dq_acc, dQ, false, s)) ||
+            (st = launch_cast_bf16((int64_t)kv_elems, dk_acc, dK, s)) ||
+            (st = launch_cast_bf16((int64_t)kv_elems, dv_acc, dV, s)))
+            return st;
+        count_launch(DFA_KERNEL_CONVERT, 3);
+        return DFA_OK;
+    }
     const int workers = std::min(num_sms(), B * H_kv * units);
     const CachedList* c = get_list(B * H_kv, units, workers, sched);
     if (!c) return fail(DFA_ERR_CUDA, "could not build the work list");

@@ -71,6 +71,8 @@ dfa_status launch_bwd_prep_varlen(int n_seq, int H, int64_t T, int64_t P, int D,
                                   cudaStream_t s);
 dfa_status launch_convert_varlen(int n_seq, int H, int64_t T, int64_t P, int D, float scale, const int32_t* seq,
                                  const float* acc, void* out, cudaStream_t s);
+// out[i] = bf16(in[i]) for n elements (n a multiple of 8; 16-byte aligned).
+dfa_status launch_cast_bf16(int64_t n, const float* in, void* out, cudaStream_t s);
 // out[b, s, h, :] = scale * acc[b, h, s, :] cast to dt (acc is the head-major
 // fp32 dQ accumulator of the tensor-core backward; D a multiple of 8).
 // With accumulate, out is fp32 and the scaled values are added to it.
@@ -83,7 +85,8 @@ struct WorkList {
     const int32_t* items;    // [n_items], device: row * n_units + unit
     int n_workers;
     int n_units;
-    // Forward split-kv items (dfa_build_split_worklist): values are
+    // Split-kv items (dfa_build_split_worklist for the forward,
+    // dfa_build_bwd_split_worklist for the backward): values are
     // (row * n_units + unit) * n_split + piece; 1 / 0 without pieces.
     int n_split = 1;
     int piece_tiles = 0;

@@ -64,6 +64,8 @@ def _load() -> ctypes.CDLL:
         "dfa_chunk_schedule": (i32, [i32, i32, i32, p32]),
         "dfa_split_piece_tiles": (i32, [i32, i32, i32, i32, i32]),
         "dfa_build_varlen_worklist": (i64, [i32, p32, i32, i32, i32, i32, p32, p32]),
+        "dfa_split_bwd_piece_tiles": (i32, [i32, i32, i32, i32, i32]),
+        "dfa_build_bwd_split_worklist": (i64, [i32, i32, i32, i32, i32, p32, p32]),
         "dfa_attn_varlen_workspace_size": (sz, [p32, i32, i32, i32, i32, i32]),
         "dfa_attn_fwd_varlen": (i32, [vp, vp, vp, i32, p32, i32, i32, i32, i32, i32, f32, vp, vp, vp, sz, vp]),
         "dfa_attn_bwd_varlen": (i32, [vp, vp, vp, vp, vp, vp, i32, p32, i32, i32, i32, i32, i32, f32,
@@ -416,6 +418,24 @@ def dfa_build_split_worklist(n_rows: int, n_units: int, kv_tiles: int, causal: b
                                        offsets.ctypes.data_as(p32), items.ctypes.data_as(p32))
     if mk < 0:
         raise DfaError(DFA_ERR_INVALID_ARG, "bad split work-list arguments")
+    return offsets, items[: offsets[-1]], int(mk)
+
+
+def dfa_split_bwd_piece_tiles(B: int, H_kv: int, S: int, causal: bool, n_sms: int) -> int:
+    """Host-only: the backward split-kv piece length (query tiles), 0 if not split."""
+    return int(_lib.dfa_split_bwd_piece_tiles(B, H_kv, S, int(bool(causal)), n_sms))
+
+
+def dfa_build_bwd_split_worklist(n_rows: int, kv_tiles: int, causal: bool, piece_tiles: int, n_workers: int):
+    """Host-only: backward split-kv pieces dealt to workers -> (offsets, items, makespan)."""
+    import numpy as np
+    n_split = max(1, -(-kv_tiles // piece_tiles)) if piece_tiles > 0 else 1
+    offsets = np.zeros(n_workers + 1, dtype=np.int32)
+    items = np.zeros(max(n_rows * kv_tiles * n_split, 1), dtype=np.int32)
+    mk = _lib.dfa_build_bwd_split_worklist(n_rows, kv_tiles, int(bool(causal)), piece_tiles, n_workers,
+                                           _p32(offsets), _p32(items))
+    if mk < 0:
+        raise DfaError(DFA_ERR_INVALID_ARG, "bad backward split work-list arguments")
     return offsets, items[: offsets[-1]], int(mk)
 
 

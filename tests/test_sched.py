@@ -179,3 +179,53 @@ def test_varlen_workspace_and_worklist_reject_bad_offsets():
     assert dfa.dfa_attn_varlen_workspace_size([0], 4, 2, 128, True) > 0
     with pytest.raises(dfa.DfaError):
         dfa.dfa_build_varlen_worklist([3, 5], 2, 4, True, 4)   # a sequence above n_units_max
+
+
+# ---------------------------------------------------------------- backward split-kv
+@pytest.mark.parametrize("B,Hkv,S,causal,n_sms", [(1, 1, 4096, True, 152), (1, 1, 8192, True, 152),
+                                                  (1, 1, 16384, True, 152), (1, 1, 4096, False, 152),
+                                                  (2, 1, 8192, True, 148)])
+def test_split_bwd_piece_tiles(B, Hkv, S, causal, n_sms):
+    piece = dfa.dfa_split_bwd_piece_tiles(B, Hkv, S, causal, n_sms)
+    n = -(-S // 128)
+    work = B * Hkv * (n * (n + 1) // 2 if causal else n * n)
+    assert piece == max(16, -(-work // (2 * n_sms)))
+    assert -(-n // piece) >= 2
+
+
+@pytest.mark.parametrize("B,Hkv,S,n_sms", [(1, 32, 131072, 152), (1, 1, 1024, 152), (1, 8, 65536, 152), (0, 1, 4096, 152)])
+def test_split_bwd_not_used_on_large_or_short_problems(B, Hkv, S, n_sms):
+    assert dfa.dfa_split_bwd_piece_tiles(B, Hkv, S, True, n_sms) == 0
+
+
+def test_split_bwd_needs_a_quarter_of_the_sms_idle():
+    # 128 key tiles per row: 64 mirror pairs per row
+    assert dfa.dfa_split_bwd_piece_tiles(1, 1, 16384, True, 152) > 0       # 64 pairs
+    assert dfa.dfa_split_bwd_piece_tiles(1, 2, 16384, True, 152) == 0      # 128 pairs > 114
+    assert dfa.dfa_split_bwd_piece_tiles(1, 1, 24576, True, 152) > 0       # 96 pairs
+
+
+@pytest.mark.parametrize("rows,n,causal,piece,W", [(1, 32, True, 16, 152), (1, 64, True, 16, 152),
+                                                   (1, 128, True, 28, 152), (2, 32, False, 16, 64), (3, 9, True, 4, 5)])
+def test_bwd_split_worklist_covers_every_visible_tile_pair_once(rows, n, causal, piece, W):
+    offsets, items, makespan = dfa.dfa_build_bwd_split_worklist(rows, n, causal, piece, W)
+    n_split = -(-n // piece)
+    assert offsets[0] == 0 and np.all(np.diff(offsets) >= 0) and offsets[-1] == len(items)
+    seen, cost = set(), []
+    for w in range(W):
+        c = 0
+        for it in items[offsets[w]:offsets[w + 1]].tolist():
+            s, ru = it % n_split, it // n_split
+            row, u = ru // n, ru % n
+            t = n - 1 - u
+            lo_i = t if causal else 0
+            lo, hi = lo_i + s * piece, min(n, lo_i + (s + 1) * piece)
+            assert lo < hi, "empty pieces are not listed"
+            for i in range(lo, hi):
+                assert (row, t, i) not in seen
+                seen.add((row, t, i))
+            c += hi - lo
+        cost.append(c)
+    assert seen == {(r, t, i) for r in range(rows) for t in range(n) for i in range(t if causal else 0, n)}
+    assert makespan == max(cost)
+    assert makespan <= sum(cost) / W + piece

@@ -113,3 +113,35 @@ def test_split_kv_long_single_head_agrees_with_sampled_oracle_rows():
     el = np.max(np.abs(np64(lse[0, 0, rows]) - lr))
     assert eo <= 2e-2, f"32K sampled rows: O err {eo}"
     assert el <= 1e-3, f"32K sampled rows: lse err {el}"
+
+
+BWD_CASES = [
+    # (B, H, Hkv, S, causal): few key-tile pairs, so the backward splits every key tile's query range
+    (1, 1, 1, 4096, True),
+    (1, 1, 1, 8192, True),
+    (1, 2, 1, 16384, True),     # GQA: the pieces of one key tile cover both heads of the group
+    (1, 1, 1, 4096, False),
+]
+
+
+@pytest.mark.parametrize("case", BWD_CASES)
+def test_split_kv_backward_pieces_match_oracle(case):
+    B, H, Hkv, S, causal = case
+    D = 128
+    assert dfa.dfa_split_bwd_piece_tiles(B, Hkv, S, causal, n_sms()) > 0, "case must be split"
+    q, k, v, do = make(B, H, Hkv, S, D, torch.bfloat16, seed=43, device=DEV)
+    O, lse = dfa.dfa_attn_fwd(q, k, v, causal=causal)
+    conv = dfa.dfa_launch_count("convert")
+    grads = dfa.dfa_attn_bwd(q, k, v, O, lse, do, causal=causal, sched="split_kv")
+    dfa.dfa_check_errors()
+    assert dfa.dfa_launch_count("convert") == conv + 3, "dQ convert and the dK, dV casts"
+    ref_grads = dfa.dfa_attn_bwd(q, k, v, O, lse, do, causal=causal, sched="balanced")
+    dfa.dfa_check_errors()
+    for name, g, r in zip(("dQ", "dK", "dV"), grads, ref_grads):
+        scale = torch.max(torch.abs(r.float())).item()
+        assert torch.max(torch.abs(g.float() - r.float())).item() <= 2e-2 * scale, f"{case}: {name} vs balanced"
+    if S <= 8192:
+        ref = oracle.attn_bwd(np64(q), np64(k), np64(v), np64(do), causal=causal)
+        for name, g, r in zip(("dQ", "dK", "dV"), grads, ref):
+            rel = np.max(np.abs(np64(g) - r)) / max(np.max(np.abs(r)), 1e-2)
+            assert rel <= 3e-2, f"{case}: {name} rel err {rel}"
