@@ -234,6 +234,14 @@ dfa_status dfa_attn_fwd_noalloc(const void* q, const void* k, const void* v, dfa
                                 int B, int H, int H_kv, int S, int D, int n_chunks, int causal,
                                 float scale, dfa_sched sched, void* O, float* lse, void* stream);
 
+/* Releases what the library keeps between calls: the pinned host copies of
+ * the work lists it has built (one per problem shape and schedule) and the
+ * pinned staging buffers and events of the packed-batch calls.  Waits for the
+ * last copy out of each staging buffer.  No device memory is held.  Call it
+ * only when no call of this library is running on another host thread;
+ * later calls rebuild what they need. */
+void dfa_shutdown(void);
+
 /* Synchronises `stream`, then reports and clears the device error flag:
  * DFA_ERR_TIMEOUT if a kernel gave up on a bounded wait, DFA_ERR_CUDA if the
  * stream holds a CUDA error, DFA_OK otherwise. */

@@ -806,6 +806,26 @@ extern "C" dfa_status dfa_attn_bwd_varlen(const void* q, const void* k, const vo
     return st;
 }
 
+extern "C" void dfa_shutdown(void) {
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        for (auto& kv : g_lists) cudaFreeHost(kv.second.host);
+        for (auto& kv : g_split_lists) cudaFreeHost(kv.second.host);
+        for (auto& kv : g_bwd_split_lists) cudaFreeHost(kv.second.host);
+        g_lists.clear();
+        g_split_lists.clear();
+        g_bwd_split_lists.clear();
+    }
+    std::lock_guard<std::mutex> lk(g_stage_mu);
+    for (auto& dev : g_stage)
+        for (Stage& st : dev) {
+            if (st.pending) cudaEventSynchronize(st.ev);
+            if (st.host) cudaFreeHost(st.host);
+            if (st.ev) cudaEventDestroy(st.ev);
+            st = Stage{};
+        }
+}
+
 extern "C" dfa_status dfa_check_errors(void* stream) {
     g_msg[0] = 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

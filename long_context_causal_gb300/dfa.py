@@ -58,6 +58,7 @@ def _load() -> ctypes.CDLL:
                                      vp, vp, vp, vp, sz, vp]),
         "dfa_attn_fwd_noalloc": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, f32, i32, vp, vp, vp]),
         "dfa_check_errors": (i32, [vp]),
+        "dfa_shutdown": (None, []),
         "dfa_last_error": (ctypes.c_char_p, []),
         "dfa_launch_count": (i64, [i32]),
         "dfa_build_worklist": (i64, [i32, i32, i32, i32, p32, p32]),
@@ -374,6 +375,11 @@ def dfa_debug_cta_trace(buf=None):
     else:
         _check(_lib.dfa_debug_cta_trace(_ptr(buf), buf.numel() // 16))
     return buf
+
+
+def dfa_shutdown():
+    """Releases the library's cached pinned work lists and staging buffers."""
+    _lib.dfa_shutdown()
 
 
 def dfa_check_errors(stream=None):

@@ -112,3 +112,18 @@ def test_empty_batch_and_bad_offsets():
     with pytest.raises(dfa.DfaError) as e:
         dfa.dfa_attn_fwd_varlen(q.float(), k.float(), v.float(), cu)
     assert e.value.status == dfa.DFA_ERR_UNSUPPORTED
+
+
+def test_shutdown_releases_caches_and_later_calls_rebuild_them():
+    q, k, v, do, cu = packed([700, 300], 2, 2, 128, seed=71)
+    O1, l1 = dfa.dfa_attn_fwd_varlen(q, k, v, cu)
+    g1 = dfa.dfa_attn_bwd_varlen(q, k, v, O1, l1, do, cu)
+    Od1, ld1 = dfa.dfa_attn_fwd(q[None], k[None], v[None], sched="split_kv")
+    torch.cuda.synchronize()
+    dfa.dfa_shutdown()
+    O2, l2 = dfa.dfa_attn_fwd_varlen(q, k, v, cu)
+    g2 = dfa.dfa_attn_bwd_varlen(q, k, v, O2, l2, do, cu)
+    Od2, ld2 = dfa.dfa_attn_fwd(q[None], k[None], v[None], sched="split_kv")
+    dfa.dfa_check_errors()
+    assert torch.equal(O1, O2) and torch.equal(l1, l2) and torch.equal(Od1, Od2) and torch.equal(ld1, ld2)
+    assert torch.equal(g1[1], g2[1]) and torch.equal(g1[2], g2[2])
