@@ -43,6 +43,15 @@ dfa_status dfa_debug_mma(int form, const void* A, const void* B, float* C, void*
  * the buffer and must keep it alive while tracing is on. */
 dfa_status dfa_debug_cta_trace(uint64_t* buf, int capacity);
 
+/* Failure detection without a GPU fault: launches one CTA of two warps that
+ * wait on mbarriers nothing ever arrives on, through the same bounded wait
+ * the attention kernels use (4 s).  The first warp gives up, raises the
+ * CTA's abort flag and the device error flag; the second leaves on the abort
+ * flag.  The kernel then returns normally, so the context stays usable, and
+ * dfa_check_errors() reports DFA_ERR_TIMEOUT (and clears the flag).  If `out`
+ * (device, 2 ints) is given, out[w] = 1 if warp w's wait completed, else 0. */
+dfa_status dfa_debug_wait_timeout(int* out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,6 +1,8 @@
-// tc_selftest.cu -- one 128x128x128 tcgen05 product per operand form (see
-// include/dfa_debug.h).  Uses exactly the descriptors, swizzle and TMEM
-// layouts of the attention kernels, so each form can be checked on its own.
+// tc_selftest.cu -- bring-up hooks of include/dfa_debug.h: one 128x128x128
+// tcgen05 product per operand form (exactly the descriptors, swizzle and TMEM
+// layouts of the attention kernels, so each form can be checked on its own),
+// and a kernel whose bounded waits run out, to test failure detection
+// without faulting or hanging the GPU.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -111,8 +113,38 @@ mma_selftest_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
+// Two warps wait on mbarriers that nothing ever arrives on, through the same
+// bounded wait as the attention kernels.  Warp 0 gives up after the limit and
+// raises the CTA's abort flag and the device error flag; warp 1 (no error
+// flag of its own) leaves on the abort flag or on its own limit, as the other
+// roles of a CTA do.  out[w] = 1 if warp w's wait completed, 0 if it gave up.
+__global__ void __launch_bounds__(64, 1) wait_timeout_kernel(int* err, int* out) {
+    __shared__ uint64_t bars[2];
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const int warp = threadIdx.x / 32;
+    const bool ok = mbar_wait(&bars[warp], 0, &abort_flag, warp == 0 ? err : nullptr);
+    if (out && (threadIdx.x & 31) == 0) out[warp] = ok ? 1 : 0;
+}
+
 }  // namespace
 }  // namespace dfa
+
+extern "C" dfa_status dfa_debug_wait_timeout(int* out, void* stream) {
+    using namespace dfa;
+    if (out && (reinterpret_cast<uintptr_t>(out) & 3u)) return fail(DFA_ERR_INVALID_ARG, "misaligned out");
+    int* err = device_error_flag();
+    if (!err) return fail(DFA_ERR_CUDA, "device error flag unavailable");
+    wait_timeout_kernel<<<1, 64, 0, static_cast<cudaStream_t>(stream)>>>(err, out);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? DFA_OK : fail(DFA_ERR_CUDA, "wait-timeout launch: %s", cudaGetErrorString(e));
+}
 
 extern "C" dfa_status dfa_debug_mma(int form, const void* A, const void* B, float* C, void* stream) {
     using namespace dfa;

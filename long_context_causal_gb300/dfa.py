@@ -74,6 +74,7 @@ def _load() -> ctypes.CDLL:
         "dfa_build_split_worklist": (i64, [i32, i32, i32, i32, i32, i32, p32, p32]),
         "dfa_debug_mma": (i32, [i32, vp, vp, vp, vp]),
         "dfa_debug_cta_trace": (i32, [vp, i32]),
+        "dfa_debug_wait_timeout": (i32, [vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -380,6 +381,12 @@ def dfa_debug_cta_trace(buf=None):
 def dfa_shutdown():
     """Releases the library's cached pinned work lists and staging buffers."""
     _lib.dfa_shutdown()
+
+
+def dfa_debug_wait_timeout(out=None, stream=None):
+    """Launches the bounded-wait timeout kernel (out: optional int32 CUDA tensor of 2)."""
+    _check(_lib.dfa_debug_wait_timeout(_ptr(out), _stream(stream)))
+    return out
 
 
 def dfa_check_errors(stream=None):
