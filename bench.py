@@ -271,6 +271,29 @@ def chunk_step_timing(w, q, k, v, O, lse, do, stream, dfa, reps=5):
             res[f"{tag}_ms"] = ms
             res[f"{tag}_tflops"] = pairs * w.D * per_pair / (ms * 1e-3) / 1e12
         out[name] = res
+        if name == "off_diagonal":   # keep this step's partial for the merge below
+            Op_first, lp_first = Op.clone(), lp.clone()
+    # The owner's merge of two chunk partials (rescale-and-merge): HBM-bound,
+    # three [B, C, H, D] fp32 tensors and three [B, H, C] lse per call.
+    Om, lm = torch.empty_like(Op), torch.empty_like(lp)
+
+    def merge():
+        dfa.dfa_merge_partials(Op_first, lp_first, Op, lp, O_out=Om, lse_out=lm, stream=stream)
+    for _ in range(2):
+        merge()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(q.device)
+    a.record(stream)
+    for _ in range(reps):
+        merge()
+    b.record(stream)
+    torch.cuda.synchronize(q.device)
+    ms = a.elapsed_time(b) / reps
+    nbytes = 3 * (Op.numel() + lp.numel()) * 4
+    peaks, kind = measured_peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    out["merge"] = {"ms": ms, "bytes": nbytes, "gbs": gbs, "frac_of_hbm_peak": gbs / float(peaks["hbm_gbs"]),
+                    "peak_kind": kind}
     dfa.dfa_check_errors(stream)
     return out
 
