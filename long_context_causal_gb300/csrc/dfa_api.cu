@@ -673,11 +673,11 @@ bool varlen_layout(const int32_t* cu, int n, int H, int Hkv, int D, bool bwd, Va
 }
 
 // Builds [token starts | padded starts | offsets | items] in a staging buffer
-// and copies it to the workspace on `s`.  Returns the worker count (0 on error).
-int upload_varlen(const int32_t* cu, int n, int unit_rows, int heads, int causal, const VarlenLayout& L,
-                  char* ws, cudaStream_t s) {
+// and copies it to the workspace on `s`; *workers receives the worker count.
+dfa_status upload_varlen(const int32_t* cu, int n, int unit_rows, int heads, int causal, const VarlenLayout& L,
+                         char* ws, cudaStream_t s, int* workers_out) {
     const int dev = current_device();
-    if (dev < 0) return fail(DFA_ERR_CUDA, "no current device"), 0;
+    if (dev < 0) return fail(DFA_ERR_CUDA, "no current device");
     const int workers = (int)std::max<int64_t>(1, std::min<int64_t>(num_sms(), L.items));
     const size_t head = 2 * ((size_t)n + 1), count = head + workers + 1 + (size_t)L.items;
     std::vector<int32_t> units(n);
@@ -685,18 +685,18 @@ int upload_varlen(const int32_t* cu, int n, int unit_rows, int heads, int causal
     std::lock_guard<std::mutex> lk(g_stage_mu);
     Stage& st = g_stage[dev][g_stage_next[dev]++ % kStages];
     if (st.pending) {
-        if (cudaEventSynchronize(st.ev) != cudaSuccess) return fail(DFA_ERR_CUDA, "staging event"), 0;
+        if (cudaEventSynchronize(st.ev) != cudaSuccess) return fail(DFA_ERR_CUDA, "staging event");
         st.pending = false;
     }
     if (!st.ev && cudaEventCreateWithFlags(&st.ev, cudaEventDisableTiming) != cudaSuccess)
-        return fail(DFA_ERR_CUDA, "staging event"), 0;
+        return fail(DFA_ERR_CUDA, "staging event");
     if (st.cap < count) {
         if (st.host) cudaFreeHost(st.host);
         st.host = nullptr;
         st.cap = 0;
         const size_t cap = std::max<size_t>(count, 4096);
         if (cudaHostAlloc((void**)&st.host, cap * sizeof(int32_t), cudaHostAllocDefault) != cudaSuccess)
-            return fail(DFA_ERR_CUDA, "pinned staging buffer of %zu bytes", cap * sizeof(int32_t)), 0;
+            return fail(DFA_ERR_CUDA, "pinned staging buffer of %zu bytes", cap * sizeof(int32_t));
         st.cap = cap;
     }
     int32_t* h = st.host;
@@ -708,12 +708,13 @@ int upload_varlen(const int32_t* cu, int n, int unit_rows, int heads, int causal
     }
     if (dfa_build_varlen_worklist(n, units.data(), heads, std::max(L.units_max, 1), causal, workers, h + head,
                                   h + head + workers + 1) < 0)
-        return fail(DFA_ERR_INVALID_ARG, "could not build the packed-batch work list"), 0;
+        return fail(DFA_ERR_INVALID_ARG, "could not build the packed-batch work list");
     cudaError_t e = cudaMemcpyAsync(ws + L.seq, h, count * sizeof(int32_t), cudaMemcpyHostToDevice, s);
-    if (e != cudaSuccess) return fail(DFA_ERR_CUDA, "packed-batch upload: %s", cudaGetErrorString(e)), 0;
-    if (cudaEventRecord(st.ev, s) != cudaSuccess) return fail(DFA_ERR_CUDA, "staging event record"), 0;
+    if (e != cudaSuccess) return fail(DFA_ERR_CUDA, "packed-batch upload: %s", cudaGetErrorString(e));
+    if (cudaEventRecord(st.ev, s) != cudaSuccess) return fail(DFA_ERR_CUDA, "staging event record");
     st.pending = true;
-    return workers;
+    *workers_out = workers;
+    return DFA_OK;
 }
 
 AttnProblem varlen_problem(int n, int H, int Hkv, int64_t T, int D, int causal, float scale, const int32_t* seq) {
@@ -763,8 +764,8 @@ extern "C" dfa_status dfa_attn_fwd_varlen(const void* q, const void* k, const vo
     if ((st = check_ptrs({q, k, v, O, lse}))) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char* ws = static_cast<char*>(workspace);
-    const int workers = upload_varlen(cu_seqlens, n_seq, kFwdUnitRows, H, causal, L, ws, s);
-    if (!workers) return DFA_ERR_CUDA;
+    int workers = 0;
+    if ((st = upload_varlen(cu_seqlens, n_seq, kFwdUnitRows, H, causal, L, ws, s, &workers))) return st;
     const int32_t* seq = reinterpret_cast<const int32_t*>(ws + L.seq);
     const int32_t* wl_dev = reinterpret_cast<const int32_t*>(ws + L.wl);
     const AttnProblem p = varlen_problem(n_seq, H, H_kv, L.T, D, causal, scale, seq);
@@ -786,8 +787,8 @@ extern "C" dfa_status dfa_attn_bwd_varlen(const void* q, const void* k, const vo
     if ((st = check_ptrs({q, k, v, O, lse, dO, dQ, dK, dV}))) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char* ws = static_cast<char*>(workspace);
-    const int workers = upload_varlen(cu_seqlens, n_seq, kBwdUnitRows, H_kv, causal, L, ws, s);
-    if (!workers) return DFA_ERR_CUDA;
+    int workers = 0;
+    if ((st = upload_varlen(cu_seqlens, n_seq, kBwdUnitRows, H_kv, causal, L, ws, s, &workers))) return st;
     const int32_t* seq = reinterpret_cast<const int32_t*>(ws + L.seq);
     const int32_t* wl_dev = reinterpret_cast<const int32_t*>(ws + L.wl);
     float* delta = reinterpret_cast<float*>(ws + L.delta);
