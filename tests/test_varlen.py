@@ -127,3 +127,24 @@ def test_shutdown_releases_caches_and_later_calls_rebuild_them():
     dfa.dfa_check_errors()
     assert torch.equal(O1, O2) and torch.equal(l1, l2) and torch.equal(Od1, Od2) and torch.equal(ld1, ld2)
     assert torch.equal(g1[1], g2[1]) and torch.equal(g1[2], g2[2])
+
+
+def test_batches_of_empty_and_of_one_token_sequences():
+    q, k, v, do, cu = packed([64], 2, 2, 128, seed=97)
+    O, lse = dfa.dfa_attn_fwd_varlen(q[:0], k[:0], v[:0], [0, 0, 0])      # three empty sequences
+    g = dfa.dfa_attn_bwd_varlen(q[:0], k[:0], v[:0], O, lse, do[:0], [0, 0, 0])
+    dfa.dfa_check_errors()
+    assert O.shape[0] == 0 and all(t.shape[0] == 0 for t in g)
+    q, k, v, do, cu = packed([1] * 7, 4, 2, 128, seed=101)                 # seven one-token sequences
+    O, lse = dfa.dfa_attn_fwd_varlen(q, k, v, cu)
+    dQ, dK, dV = dfa.dfa_attn_bwd_varlen(q, k, v, O, lse, do, cu)
+    dfa.dfa_check_errors()
+    # One token sees only itself: O = v of its group, P = 1 so dS = 0 (dQ = dK = 0) and dV = sum of dO over the group.
+    G = 2
+    vg = v.float().repeat_interleave(G, dim=1)
+    assert torch.max(torch.abs(O.float() - vg)).item() <= 1e-2
+    Or, lr = oracle.attn_fwd_varlen(np64(q), np64(k), np64(v), cu)
+    assert np.max(np.abs(np64(lse) - lr)) <= 1e-3
+    assert torch.max(torch.abs(dQ.float())).item() <= 1e-2 and torch.max(torch.abs(dK.float())).item() <= 1e-2
+    dv_ref = do.float().view(7, 2, G, 128).sum(dim=2)
+    assert torch.max(torch.abs(dV.float() - dv_ref)).item() <= 2e-2 * max(torch.max(torch.abs(dv_ref)).item(), 1.0)
