@@ -68,12 +68,13 @@ typedef enum { DFA_F32 = 0, DFA_BF16 = 1 } dfa_dtype;
  *   tiles; each piece is an item of its own whose fp32 partial (O, lse) goes
  *   to the workspace, and a merge kernel combines each row's pieces with the
  *   rescale-and-merge rule.  In a bf16 head-dim-128 backward whose mirror
- *   pairs of key tiles number at most 3/4 of the SMs, every key tile's query range is cut
- *   into pieces of dfa_split_bwd_piece_tiles() query tiles, and each piece
- *   adds its partial dK, dV to fp32 accumulators in the workspace (vector
- *   reductions), cast to bf16 at the end.  Larger problems, the local
- *   window, fp32 I/O, head dim 64 and the no-alloc forward treat it as
- *   BALANCED. */
+ *   pairs of key tiles number at most 3/4 of the SMs, every key tile's
+ *   query range is cut into pieces of dfa_split_bwd_piece_tiles() query
+ *   tiles (§3.3: a helper computes part of a worker's gradients), and each
+ *   piece adds its partial dK, dV to fp32 accumulators in the workspace
+ *   (vector reductions), cast to bf16 at the end.  Larger problems, the
+ *   local window, fp32 I/O, head dim 64 (backward) and the no-alloc forward
+ *   treat it as BALANCED. */
 typedef enum { DFA_SCHED_BALANCED = 0, DFA_SCHED_UNBALANCED = 1, DFA_SCHED_SPLIT_KV = 2 } dfa_sched;
 
 /* One chunk step (DISTFLASHATTN App. D: a worker's step advances its attention
@@ -137,8 +138,10 @@ dfa_status dfa_chunk_attn_bwd(const void* q, const void* k, const void* v, const
 /* Bytes of workspace dfa_chunk_attn_bwd needs (0 for invalid sizes). */
 size_t dfa_chunk_bwd_workspace_size(int B, int H, int H_kv, int Lq, int Lkv, int D);
 
-/* Bytes of workspace dfa_attn_fwd (bwd = 0) or dfa_attn_bwd (bwd = 1) needs.
- * Returns 0 for invalid sizes. */
+/* Bytes of workspace dfa_attn_fwd (bwd = 0) or dfa_attn_bwd (bwd = 1) needs,
+ * for every schedule: on a problem small enough for SPLIT_KV it includes the
+ * pieces' fp32 partials (forward) or dK/dV accumulators (backward), sized
+ * for the current device's SM count.  Returns 0 for invalid sizes. */
 size_t dfa_attn_workspace_size(int B, int H, int H_kv, int S, int D, int n_chunks, int bwd);
 
 /* Whole-sequence causal forward over n_chunks token chunks (DISTFLASHATTN §3.1,
