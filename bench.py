@@ -40,7 +40,7 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--shape", default=None,
                     help="B,H,H_kv,S,D: a custom bf16 shape instead of a named workload (profiling cases)")
-    ap.add_argument("--sched", choices=["balanced", "unbalanced"], default="balanced")
+    ap.add_argument("--sched", choices=["balanced", "unbalanced", "split_kv"], default="balanced")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-chunk-step", action="store_true", help="skip the per-worker chunk-step timing")
