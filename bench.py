@@ -639,6 +639,8 @@ def main():
                    "l2": "inputs larger than L2 (each tensor exceeds 129 MB)"},
         "pct_of_nominal_bf16_peak": 100.0 * value / world / NOMINAL_BF16_TFLOPS,
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
+        # the backward counted at 8D per pair (without recomputing S = QK^T), for other conventions
+        "bwd_tflops_8d": bwd_tflops * 0.8,
         "roofline": {"bound": "tensor", "kernel": "dfa_attn_bwd (delta + bwd + dQ convert)",
                      "achieved": bwd_tflops, "peak": peak_tc, "unit": "TFLOP/s",
                      "frac": bwd_tflops / peak_tc,
