@@ -45,6 +45,8 @@ CASES = [
     (1, 2, 2, 2048, 128, False, 1.0),    # non-causal: every block sees every piece
     (2, 3, 3, 1536, 128, True, 1.0),     # batch
     (1, 4, 1, 2048, 128, True, 4.0),     # sharp softmax: pieces with very different maxima
+    (1, 8, 1, 4096, 128, True, 1.0),     # GQA 8:1
+    (2, 2, 2, 1280, 64, False, 1.0),     # D = 64, non-causal, batch, ragged
 ]
 
 

@@ -37,6 +37,8 @@ CASES = [
     ([17, 256, 255, 513], 2, 1, 64, True),               # D = 64 kernels, GQA 2:1
     ([200, 700], 2, 2, 128, False),                      # non-causal inside each sequence
     ([128, 128, 384, 4096], 8, 8, 128, True),            # tile-aligned lengths, one long sequence
+    ([4096, 100, 2000], 8, 1, 128, True),                # GQA 8:1
+    ([333, 777], 4, 4, 64, False),                       # D = 64, non-causal
 ]
 
 
