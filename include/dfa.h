@@ -160,7 +160,12 @@ dfa_status dfa_attn_fwd(const void* q, const void* k, const void* v, dfa_dtype d
  *   Delta_i = <dO_i, O_i>,  P_ij = exp(s_ij - lse_i),  dS_ij = P_ij (dO_i.v_j - Delta_i)
  *   dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO  (dK, dV summed over a GQA group).
  * Same layouts as dfa_attn_fwd; dQ/dK/dV are written (not accumulated) in dt.
- * The workspace holds the fp32 dQ accumulator and Delta. */
+ * The workspace holds the fp32 dQ accumulator and Delta.
+ * Reproducibility: O and lse of the forward, and dK, dV of the backward
+ * under BALANCED and UNBALANCED, are the same bits on every call (one CTA
+ * owns each output row).  dQ adds fp32 partials with atomics in no fixed
+ * order, so it may differ in the last bits from call to call; so may dK and
+ * dV when SPLIT_KV cuts the backward into pieces. */
 dfa_status dfa_attn_bwd(const void* q, const void* k, const void* v, const void* O,
                         const float* lse, const void* dO, dfa_dtype dt,
                         int B, int H, int H_kv, int S, int D, int n_chunks, int causal,
