@@ -143,6 +143,29 @@ def test_merge_matches_oracle_including_empty_rows():
     assert torch.equal(Oa2, Om) and torch.equal(la2, lm)
 
 
+@pytest.mark.parametrize("shape", [(1, 5, 3, 64), (1, 7, 2, 12), (2, 3, 1, 1032), (3, 333, 5, 128)])
+def test_merge_row_groups_ragged_and_in_place(shape):
+    # Warps take groups of rows (several short rows, or chunks of one long
+    # row); the last group is ragged, and the output may alias either input.
+    B, L, H, D = shape
+    g = torch.Generator(device=DEV).manual_seed(13)
+    Oa = torch.randn((B, L, H, D), generator=g, device=DEV)
+    Ob = torch.randn((B, L, H, D), generator=g, device=DEV)
+    la = torch.randn((B, H, L), generator=g, device=DEV) * 3
+    lb = torch.randn((B, H, L), generator=g, device=DEV) * 3
+    lb[-1, -1, -1] = -float("inf")
+    Or, lr = oracle.merge(np64(Oa), np64(la), np64(Ob), np64(lb))
+    Om, lm = dfa.dfa_merge_partials(Oa, la, Ob, lb)
+    torch.cuda.synchronize()
+    assert np.max(np.abs(np64(lm) - lr)) <= 1e-5 and np.max(np.abs(np64(Om) - Or)) <= 1e-5
+    for side in ("a", "b"):
+        Oa2, la2, Ob2, lb2 = Oa.clone(), la.clone(), Ob.clone(), lb.clone()
+        Od, ld = (Oa2, la2) if side == "a" else (Ob2, lb2)
+        dfa.dfa_merge_partials(Oa2, la2, Ob2, lb2, O_out=Od, lse_out=ld)
+        torch.cuda.synchronize()
+        assert torch.equal(Od, Om) and torch.equal(ld, lm), f"in place on {side}"
+
+
 # ---------------------------------------------------------------- whole-sequence, small shapes
 SMALL = [
     # (dtype, B, H, Hkv, S, D, n_chunks)
