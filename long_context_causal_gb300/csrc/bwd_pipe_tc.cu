@@ -471,10 +471,10 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                                 __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[(c + e + w) / 2]));
                             const float2 p23 =
                                 __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[(c + e + w) / 2 + 1]));
-                            dk[w / 2] = pack_bf16(p01.x * (__uint_as_float(u[e + w]) - d4.x),
-                                                  p01.y * (__uint_as_float(u[e + w + 1]) - d4.y));
-                            dk[w / 2 + 1] = pack_bf16(p23.x * (__uint_as_float(u[e + w + 2]) - d4.z),
-                                                      p23.y * (__uint_as_float(u[e + w + 3]) - d4.w));
+                            dk[w / 2] = ds_pack_bf16(p01.x, p01.y, __uint_as_float(u[e + w]),
+                                                     __uint_as_float(u[e + w + 1]), d4.x, d4.y);
+                            dk[w / 2 + 1] = ds_pack_bf16(p23.x, p23.y, __uint_as_float(u[e + w + 2]),
+                                                         __uint_as_float(u[e + w + 3]), d4.z, d4.w);
                         }
                         *reinterpret_cast<uint4*>(blk + sw128_offset(r, c + e)) = make_uint4(dk[0], dk[1], dk[2], dk[3]);
                     }

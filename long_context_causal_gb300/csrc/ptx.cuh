@@ -426,6 +426,25 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return r;
 }
 
+// Two softmax-gradient entries packed to bf16x2, `lo` = p0 (u0 - d0) and
+// `hi` = p1 (u1 - d1), with the two-lane fp32 instructions of sm_100 and later
+// (sub.f32x2, mul.f32x2): each lane is rounded exactly as the scalar
+// subtract and multiply, in half the instructions.
+__device__ __forceinline__ uint32_t ds_pack_bf16(float p0, float p1, float u0, float u1, float d0, float d1) {
+    uint32_t r;
+    asm("{\n\t.reg .b64 a, b, c;\n\t.reg .f32 lo, hi;\n\t"
+        "mov.b64 a, {%1, %2};\n\t"
+        "mov.b64 b, {%3, %4};\n\t"
+        "sub.rn.f32x2 a, a, b;\n\t"
+        "mov.b64 c, {%5, %6};\n\t"
+        "mul.rn.f32x2 a, a, c;\n\t"
+        "mov.b64 {lo, hi}, a;\n\t"
+        "cvt.rn.bf16x2.f32 %0, hi, lo;\n\t}"
+        : "=r"(r)
+        : "f"(u0), "f"(u1), "f"(d0), "f"(d1), "f"(p0), "f"(p1));
+    return r;
+}
+
 // Byte offset of element (row, col) of a [rows][64] bf16 block stored with the
 // 128-byte swizzle: 16-byte chunk index XOR (row mod 8).
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t col) {
