@@ -112,7 +112,7 @@ delta_kernel(int B, int H, int S, int D, const T* __restrict__ O, const T* __res
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 bwd_prep_kernel(int B, int H, int S, int S_pad, int D, const T* __restrict__ O, const T* __restrict__ dO,
-                const float* __restrict__ lse, float* __restrict__ lse2, float* __restrict__ delta) {
+                const float* __restrict__ lse, float* __restrict__ nlse2, float* __restrict__ delta) {
     const int64_t row = (int64_t)blockIdx.x * (kThreads / 32) + threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     if (row >= (int64_t)B * S_pad * H) return;
@@ -122,7 +122,7 @@ bwd_prep_kernel(int B, int H, int S, int S_pad, int D, const T* __restrict__ O, 
     const int64_t dst = ((int64_t)b * H + h) * S_pad + i;
     if (i >= S) {
         if (lane == 0) {
-            lse2[dst] = 0.f;
+            nlse2[dst] = 0.f;
             delta[dst] = 0.f;
         }
         return;
@@ -139,7 +139,7 @@ bwd_prep_kernel(int B, int H, int S, int S_pad, int D, const T* __restrict__ O, 
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (lane == 0) {
         delta[dst] = acc;
-        lse2[dst] = lse[((int64_t)b * H + h) * S + i] * 1.4426950408889634f;
+        nlse2[dst] = lse[((int64_t)b * H + h) * S + i] * -1.4426950408889634f;   // -lse log2(e), exact negation
     }
 }
 
@@ -207,7 +207,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads)
 bwd_prep_varlen_kernel(int n, int H, int64_t Ttok, int64_t P, int D, const int32_t* __restrict__ seq,
                        const T* __restrict__ O, const T* __restrict__ dO, const float* __restrict__ lse,
-                       float* __restrict__ lse2, float* __restrict__ delta) {
+                       float* __restrict__ nlse2, float* __restrict__ delta) {
     const int64_t row = (int64_t)blockIdx.x * (kThreads / 32) + threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     if (row >= P * H) return;
@@ -218,7 +218,7 @@ bwd_prep_varlen_kernel(int n, int H, int64_t Ttok, int64_t P, int D, const int32
     const int64_t dst = (int64_t)h * P + p;
     if (rel >= seq[s + 1] - seq[s]) {
         if (lane == 0) {
-            lse2[dst] = 0.f;
+            nlse2[dst] = 0.f;
             delta[dst] = 0.f;
         }
         return;
@@ -235,7 +235,7 @@ bwd_prep_varlen_kernel(int n, int H, int64_t Ttok, int64_t P, int D, const int32
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (lane == 0) {
         delta[dst] = acc;
-        lse2[dst] = lse[(int64_t)h * Ttok + tok] * 1.4426950408889634f;
+        nlse2[dst] = lse[(int64_t)h * Ttok + tok] * -1.4426950408889634f;
     }
 }
 
@@ -353,13 +353,13 @@ dfa_status launch_merge_pieces(dfa_dtype dt, int B, int H, int S, int D, int cau
 }
 
 dfa_status launch_bwd_prep_varlen(int n_seq, int H, int64_t T, int64_t P, int D, const int32_t* seq,
-                                  const void* O, const void* dO, const float* lse, float* lse2, float* delta,
+                                  const void* O, const void* dO, const float* lse, float* nlse2, float* delta,
                                   cudaStream_t s) {
     const int64_t rows = P * H;
     if (rows == 0 || n_seq <= 0) return DFA_OK;
     const int64_t blocks = (rows + kThreads / 32 - 1) / (kThreads / 32);
     bwd_prep_varlen_kernel<__nv_bfloat16><<<(unsigned)blocks, kThreads, 0, s>>>(
-        n_seq, H, T, P, D, seq, (const __nv_bfloat16*)O, (const __nv_bfloat16*)dO, lse, lse2, delta);
+        n_seq, H, T, P, D, seq, (const __nv_bfloat16*)O, (const __nv_bfloat16*)dO, lse, nlse2, delta);
     return launched("varlen bwd prep");
 }
 
@@ -395,16 +395,16 @@ dfa_status launch_delta(dfa_dtype dt, int B, int H, int S, int D, const void* O,
 }
 
 dfa_status launch_bwd_prep(dfa_dtype dt, int B, int H, int S, int S_pad, int D, const void* O,
-                           const void* dO, const float* lse, float* lse2, float* delta, cudaStream_t s) {
+                           const void* dO, const float* lse, float* nlse2, float* delta, cudaStream_t s) {
     const int64_t rows = (int64_t)B * S_pad * H;
     if (rows == 0) return DFA_OK;
     const int64_t blocks = (rows + kThreads / 32 - 1) / (kThreads / 32);
     if (dt == DFA_F32)
         bwd_prep_kernel<float><<<(unsigned)blocks, kThreads, 0, s>>>(B, H, S, S_pad, D, (const float*)O,
-                                                                     (const float*)dO, lse, lse2, delta);
+                                                                     (const float*)dO, lse, nlse2, delta);
     else
         bwd_prep_kernel<__nv_bfloat16><<<(unsigned)blocks, kThreads, 0, s>>>(
-            B, H, S, S_pad, D, (const __nv_bfloat16*)O, (const __nv_bfloat16*)dO, lse, lse2, delta);
+            B, H, S, S_pad, D, (const __nv_bfloat16*)O, (const __nv_bfloat16*)dO, lse, nlse2, delta);
     return launched("bwd prep");
 }
 

@@ -8,7 +8,7 @@
 //
 // What differs from bwd_tc.cu is the schedule.  The softmax-gradient work of
 // a (128-key x 128-query) tile is split into two phases:
-//   phase 1  P^T = exp2(S^T c - lse2)  -- needs S^T only; P^T goes to TMEM
+//   phase 1  P^T = exp2(S^T c + nlse2)  -- needs S^T only; P^T goes to TMEM
 //            (bf16, over S^T) for dV and stays in registers (bf16 pairs);
 //   phase 2  dS^T = P^T (dP^T - Delta) -- needs dP^T; dS^T goes to swizzled
 //            shared memory for dK and dQ.
@@ -49,7 +49,7 @@ constexpr int kThreads = 512;
 constexpr int BT = 128;          // key rows per work item; query rows per tile
 constexpr int D = 128;
 constexpr int kTile = BT * D * 2;                  // 32 KB bf16 tile
-constexpr int kSide = 1024;                        // lse2[128] + Delta[128] per query tile
+constexpr int kSide = 1024;                        // nlse2[128] + Delta[128] per query tile
 constexpr int kOffK = 0, kOffV = kTile, kOffQ = 2 * kTile, kOffDO = 4 * kTile, kOffDS = 6 * kTile;
 constexpr int kOffSide = kOffDS + 32768;
 constexpr int kOffBar = kOffSide + 2 * kSide;
@@ -66,7 +66,7 @@ struct Args {
     int win_w;                    // ... and chunks per window (0: none)
     int acc_f32;                  // dK/dV: fp32 accumulate (+=) instead of bf16 store
     float scale, c2;
-    const float* lse2;
+    const float* nlse2;
     const float* delta;
     float* dq_acc;                // [B, H, acc_rows, D] fp32, zeroed by the caller
     int64_t acc_rows;             // Lq; for a packed batch the padded rows per head
@@ -262,7 +262,7 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     for (int blk = 0; blk < 2; ++blk)
                         tma_load_4d(sQ + s * kTile + blk * 16384, &tmQ, &q_full[s], blk * 64, h, SEQ_BASE(x) + i * BT,
                                     SEQ_TB(x));
-                    bulk_load(sSide + s * kSide, a.lse2 + side_off, 512, &q_full[s]);
+                    bulk_load(sSide + s * kSide, a.nlse2 + side_off, 512, &q_full[s]);
                     bulk_load(sSide + s * kSide + 512, a.delta + side_off, 512, &q_full[s]);
                 }
                 __syncwarp();
@@ -422,14 +422,14 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 const int q0 = i * BT + half * 64;
                 if (!wait(&q_full[s], (n >> 1) & 1, 0) || !wait(s_full, n & 1, 0)) break;
                 tc_fence_after();
-                const float* lse2 = reinterpret_cast<const float*>(sSide + s * kSide) + half * 64;
-                const float* dl = lse2 + BT;
+                const float* nlse2 = reinterpret_cast<const float*>(sSide + s * kSide) + half * 64;
+                const float* dl = nlse2 + BT;
                 // Elements outside the causal triangle or the sequence only occur on
                 // the diagonal tile and on ragged edges; elsewhere no mask is applied.
                 const bool full = !(a.causal && i == x.t + a.rel / BT) && (i + 1) * BT <= SEQ_LQ(x) &&
                                   (int64_t)(i + 1) * BT <= q_hi_tile &&
                                   (x.t + 1) * BT <= SEQ_LKV(x);
-                // ---- phase 1: P^T = exp2(S^T c - lse2) -> TMEM (bf16) and registers
+                // ---- phase 1: P^T = exp2(S^T c + nlse2) -> TMEM (bf16) and registers
                 uint32_t u[32], pk[32];
 #pragma unroll
                 for (int c = 0; c < 64; c += 32) {
@@ -444,11 +444,11 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     }
 #pragma unroll
                     for (int e = 0; e < 32; e += 4) {
-                        const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c + e);
-                        pk[(c + e) / 2] = pack_bf16(ex2(fmaf(__uint_as_float(u[e]), a.c2, -l4.x)),
-                                                    ex2(fmaf(__uint_as_float(u[e + 1]), a.c2, -l4.y)));
-                        pk[(c + e) / 2 + 1] = pack_bf16(ex2(fmaf(__uint_as_float(u[e + 2]), a.c2, -l4.z)),
-                                                        ex2(fmaf(__uint_as_float(u[e + 3]), a.c2, -l4.w)));
+                        const float4 l4 = *reinterpret_cast<const float4*>(nlse2 + c + e);
+                        pk[(c + e) / 2] = exp2_pack_bf16(__uint_as_float(u[e]), __uint_as_float(u[e + 1]), a.c2,
+                                                         l4.x, l4.y);
+                        pk[(c + e) / 2 + 1] = exp2_pack_bf16(__uint_as_float(u[e + 2]), __uint_as_float(u[e + 3]),
+                                                             a.c2, l4.z, l4.w);
                     }
                     tmem_st16(tS + c / 2, *reinterpret_cast<uint32_t(*)[16]>(&pk[c / 2]));
                 }
@@ -622,7 +622,7 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 }  // namespace
 
 dfa_status tc_bwd_pipelined(const AttnProblem& p, const void* q, const void* k, const void* v, const void* dO,
-                            const float* lse2, const float* delta, int S_pad, float* dq_acc, void* dK, void* dV,
+                            const float* nlse2, const float* delta, int S_pad, float* dq_acc, void* dK, void* dV,
                             bool acc_f32, const WorkList* wl, cudaStream_t s) {
     if (p.D != D) return fail(DFA_ERR_UNSUPPORTED, "pipelined backward needs D = 128");
     const int64_t rel = p.kv_offset - p.q_offset;
@@ -642,7 +642,7 @@ dfa_status tc_bwd_pipelined(const AttnProblem& p, const void* q, const void* k, 
     a.rel = (int)rel; a.acc_f32 = acc_f32;
     a.q_off = p.q_offset; a.kv_off = p.kv_offset; a.win_c = p.win_c; a.win_w = p.causal ? p.win_w : 0;
     a.scale = p.scale; a.c2 = p.scale * 1.4426950408889634f;
-    a.lse2 = lse2; a.delta = delta; a.dq_acc = dq_acc;
+    a.nlse2 = nlse2; a.delta = delta; a.dq_acc = dq_acc;
     a.dK = dK;
     a.dV = dV;
     a.wl_offsets = wl->offsets; a.wl_items = wl->items; a.n_units = wl->n_units;

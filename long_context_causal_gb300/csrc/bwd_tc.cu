@@ -20,7 +20,7 @@
 //                 S^T = K Q^T, dP^T = V dO^T, dV += P^T dO, dK += dS^T Q,
 //                 dQ = dS K (stored transposed, dQ^T = K^T dS^T, for D = 128).
 //   warp 2      TMEM allocation.
-//   warps 4-7   one key row per thread: P^T = exp2(S^T c - lse2),
+//   warps 4-7   one key row per thread: P^T = exp2(S^T c + nlse2),
 //               dS^T = P^T (dP^T - Delta); P^T (bf16) back into TMEM over S^T,
 //               dS^T (bf16) into swizzled shared memory where it serves as the
 //               K-major A operand of dK and the M-major A operand of dQ; at the
@@ -46,7 +46,7 @@ using namespace ptx;
 
 constexpr int kThreads = 384;
 constexpr int BT = 128;   // rows per query / key tile
-constexpr int kSide = 1024;   // per query slot: lse2[128] and Delta[128] (fp32)
+constexpr int kSide = 1024;   // per query slot: nlse2[128] and Delta[128] (fp32)
 
 template <int D>
 struct BCfg {
@@ -67,7 +67,7 @@ struct BwdArgs {
     int64_t win_c;                // local window: chunk length ...
     int win_w;                    // ... and chunks per window (0: none)
     float scale, c2;              // c2 = scale * log2(e)
-    const float* lse2;            // [B, H, S_pad]  lse * log2(e)
+    const float* nlse2;            // [B, H, S_pad]  -lse * log2(e)
     const float* delta;           // [B, H, S_pad]
     float* dq_acc;                // [B, H, acc_rows, D] fp32, zeroed by the caller
     int64_t acc_rows;             // S; for a packed batch the padded rows per head
@@ -247,7 +247,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     for (int blk = 0; blk < D / 64; ++blk)
                         tma_load_4d(sQ + s * C::kTile + blk * 16384, &tmQ, &q_full[s], blk * 64, h, SEQ_BASE(x) + i * BT,
                                     SEQ_TB(x));
-                    bulk_load(sSide + s * kSide, a.lse2 + side_off + i * BT, 512, &q_full[s]);
+                    bulk_load(sSide + s * kSide, a.nlse2 + side_off + i * BT, 512, &q_full[s]);
                     bulk_load(sSide + s * kSide + 512, a.delta + side_off + i * BT, 512, &q_full[s]);
                 }
                 __syncwarp();
@@ -397,8 +397,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 const uint32_t s = n & 1, ph = (n >> 1) & 1;
                 if (!wait(&q_full[s], ph, 0) || !wait(s_full, n & 1, 0) || !wait(dp_full, n & 1, 0)) break;
                 tc_fence_after();
-                const float* lse2 = reinterpret_cast<const float*>(sSide + s * kSide);
-                const float* dl = lse2 + BT;
+                const float* nlse2 = reinterpret_cast<const float*>(sSide + s * kSide);
+                const float* dl = nlse2 + BT;
                 const int q0 = i * BT;
 #pragma unroll 1
                 for (int c = 0; c < BT / 32; ++c) {
@@ -407,7 +407,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     uint32_t pk[16], dk[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 4) {
-                        const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c * 32 + e);
+                        const float4 l4 = *reinterpret_cast<const float4*>(nlse2 + c * 32 + e);
                         const float4 d4 = *reinterpret_cast<const float4*>(dl + c * 32 + e);
                         const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
                         float pp[4], dd[4];
@@ -415,7 +415,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                         for (int z = 0; z < 4; ++z) {
                             const int qg = q0 + c * 32 + e + z;
                             const bool vis = row_ok && qg < SEQ_LEN(x) && !(a.causal && kvg > qg) && qg < q_hi;
-                            const float p = vis ? ex2(fmaf(__uint_as_float(us[e + z]), a.c2, -lv[z])) : 0.f;
+                            const float p = vis ? ex2(fmaf(__uint_as_float(us[e + z]), a.c2, lv[z])) : 0.f;
                             pp[z] = p;
                             dd[z] = p * (__uint_as_float(ud[e + z]) - dv[z]);
                         }
@@ -542,7 +542,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
 template <int D>
 dfa_status launch(const AttnProblem& p, const void* q, const void* k, const void* v, const void* dO,
-                  const float* lse2, const float* delta, int S_pad, float* dq_acc, void* dK, void* dV,
+                  const float* nlse2, const float* delta, int S_pad, float* dq_acc, void* dK, void* dV,
                   const WorkList* wl, cudaStream_t s) {
     alignas(64) CUtensorMap mq, mk, mv, mdo;
     const int tB = p.seq ? 1 : p.B;   // a packed batch is one tensor row of T tokens
@@ -557,7 +557,7 @@ dfa_status launch(const AttnProblem& p, const void* q, const void* k, const void
     a.B = p.B; a.H = p.H; a.Hkv = p.Hkv; a.S = p.Lq; a.S_pad = S_pad; a.causal = p.causal;
     a.win_c = p.win_c; a.win_w = p.causal ? p.win_w : 0;
     a.scale = p.scale; a.c2 = p.scale * 1.4426950408889634f;
-    a.lse2 = lse2; a.delta = delta; a.dq_acc = dq_acc;
+    a.nlse2 = nlse2; a.delta = delta; a.dq_acc = dq_acc;
     a.dK = static_cast<__nv_bfloat16*>(dK);
     a.dV = static_cast<__nv_bfloat16*>(dV);
     a.wl_offsets = wl->offsets; a.wl_items = wl->items; a.n_units = wl->n_units;
@@ -575,12 +575,12 @@ dfa_status launch(const AttnProblem& p, const void* q, const void* k, const void
 }  // namespace
 
 dfa_status tc_bwd(const AttnProblem& p, const void* q, const void* k, const void* v, const void* dO,
-                  const float* lse2, const float* delta, int S_pad, float* dq_acc, void* dK, void* dV,
+                  const float* nlse2, const float* delta, int S_pad, float* dq_acc, void* dK, void* dV,
                   const WorkList* wl, cudaStream_t s) {
     if (p.B == 0 || p.Lq == 0) return DFA_OK;
     // Head dim 128 takes the two-stream pipelined kernel (bwd_pipe_tc.cu).
-    if (p.D == 128) return tc_bwd_pipelined(p, q, k, v, dO, lse2, delta, S_pad, dq_acc, dK, dV, false, wl, s);
-    return launch<64>(p, q, k, v, dO, lse2, delta, S_pad, dq_acc, dK, dV, wl, s);
+    if (p.D == 128) return tc_bwd_pipelined(p, q, k, v, dO, nlse2, delta, S_pad, dq_acc, dK, dV, false, wl, s);
+    return launch<64>(p, q, k, v, dO, nlse2, delta, S_pad, dq_acc, dK, dV, wl, s);
 }
 
 }  // namespace dfa

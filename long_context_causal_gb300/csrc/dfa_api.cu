@@ -135,7 +135,7 @@ const CachedList* get_bwd_split_list(int rows, int kv_tiles, int causal, int pie
 }
 
 struct Layout {
-    size_t delta = 0, lse2 = 0, dq = 0, wl = 0, opart = 0, lpart = 0, dk = 0, dv = 0, total = 0;
+    size_t delta = 0, nlse2 = 0, dq = 0, wl = 0, opart = 0, lpart = 0, dk = 0, dv = 0, total = 0;
     int S_pad = 0;
     int n_split = 1;   // split-kv pieces the workspace has room for
 };
@@ -147,7 +147,7 @@ Layout layout(int B, int H, int Hkv, int S, int D, bool bwd) {
     if (bwd) {
         L.delta = off;
         off = align_up(off + sizeof(float) * (size_t)B * H * L.S_pad);
-        L.lse2 = off;
+        L.nlse2 = off;
         off = align_up(off + sizeof(float) * (size_t)B * H * L.S_pad);
         L.dq = off;
         off = align_up(off + sizeof(float) * (size_t)B * S * H * D);
@@ -452,8 +452,8 @@ static dfa_status attn_bwd_impl(const void* q, const void* k, const void* v, con
         if (st == DFA_OK) count_launch(DFA_KERNEL_BWD, 2);
         return st;
     }
-    float* lse2 = reinterpret_cast<float*>(ws + L.lse2);
-    if ((st = launch_bwd_prep(dt, B, H, S, L.S_pad, D, O, dO, lse, lse2, delta, s))) return st;
+    float* nlse2 = reinterpret_cast<float*>(ws + L.nlse2);
+    if ((st = launch_bwd_prep(dt, B, H, S, L.S_pad, D, O, dO, lse, nlse2, delta, s))) return st;
     count_launch(DFA_KERNEL_DELTA);
     float* dq_acc = reinterpret_cast<float*>(ws + L.dq);
     cudaError_t e = cudaMemsetAsync(dq_acc, 0, sizeof(float) * (size_t)B * S * H * D, s);
@@ -481,7 +481,7 @@ static dfa_status attn_bwd_impl(const void* q, const void* k, const void* v, con
         if ((e = cudaMemsetAsync(dk_acc, 0, sizeof(float) * kv_elems, s)) != cudaSuccess ||
             (e = cudaMemsetAsync(dv_acc, 0, sizeof(float) * kv_elems, s)) != cudaSuccess)
             return fail(DFA_ERR_CUDA, "dK/dV accumulator clear: %s", cudaGetErrorString(e));
-        if ((st = tc_bwd_pipelined(p, q, k, v, dO, lse2, delta, L.S_pad, dq_acc, dk_acc, dv_acc, true, &wl, s)))
+        if ((st = tc_bwd_pipelined(p, q, k, v, dO, nlse2, delta, L.S_pad, dq_acc, dk_acc, dv_acc, true, &wl, s)))
             return st;
         count_launch(DFA_KERNEL_BWD);
         if ((st = launch_convert(dt, B, H, S, D, scale, dq_acc, dQ, false, s)) ||
@@ -497,7 +497,7 @@ static dfa_status attn_bwd_impl(const void* q, const void* k, const void* v, con
     int32_t* dev = reinterpret_cast<int32_t*>(ws + L.wl);
     if ((st = upload_list(c, dev, s))) return st;
     WorkList wl{dev, dev + workers + 1, workers, units};
-    if ((st = tc_bwd(p, q, k, v, dO, lse2, delta, L.S_pad, dq_acc, dK, dV, &wl, s))) return st;
+    if ((st = tc_bwd(p, q, k, v, dO, nlse2, delta, L.S_pad, dq_acc, dK, dV, &wl, s))) return st;
     count_launch(DFA_KERNEL_BWD);
     st = launch_convert(dt, B, H, S, D, scale, dq_acc, dQ, false, s);
     if (st == DFA_OK) count_launch(DFA_KERNEL_CONVERT);
@@ -525,7 +525,7 @@ extern "C" dfa_status dfa_attn_bwd_local(const void* q, const void* k, const voi
 
 // ---------------------------------------------------------------- chunk-pair backward
 struct ChunkLayout {
-    size_t delta = 0, lse2 = 0, dq = 0, wl = 0, total = 0;
+    size_t delta = 0, nlse2 = 0, dq = 0, wl = 0, total = 0;
     int Lq_pad = 0;
 };
 
@@ -535,7 +535,7 @@ ChunkLayout chunk_layout(int B, int H, int Hkv, int Lq, int Lkv, int D) {
     L.Lq_pad = (Lq + kBwdUnitRows - 1) / kBwdUnitRows * kBwdUnitRows;
     L.delta = off;
     off = align_up(off + sizeof(float) * (size_t)B * H * L.Lq_pad);
-    L.lse2 = off;
+    L.nlse2 = off;
     off = align_up(off + sizeof(float) * (size_t)B * H * L.Lq_pad);
     L.dq = off;
     off = align_up(off + sizeof(float) * (size_t)B * Lq * H * D);
@@ -583,8 +583,8 @@ extern "C" dfa_status dfa_chunk_attn_bwd(const void* q, const void* k, const voi
         if (st == DFA_OK) count_launch(DFA_KERNEL_BWD, 2);
         return st;
     }
-    float* lse2 = reinterpret_cast<float*>(ws + L.lse2);
-    if ((st = launch_bwd_prep(dt, B, H, Lq, L.Lq_pad, D, O, dO, lse, lse2, delta, s))) return st;
+    float* nlse2 = reinterpret_cast<float*>(ws + L.nlse2);
+    if ((st = launch_bwd_prep(dt, B, H, Lq, L.Lq_pad, D, O, dO, lse, nlse2, delta, s))) return st;
     count_launch(DFA_KERNEL_DELTA);
     float* dq = reinterpret_cast<float*>(ws + L.dq);
     cudaError_t e = cudaMemsetAsync(dq, 0, sizeof(float) * (size_t)B * Lq * H * D, s);
@@ -596,7 +596,7 @@ extern "C" dfa_status dfa_chunk_attn_bwd(const void* q, const void* k, const voi
     int32_t* dev = reinterpret_cast<int32_t*>(ws + L.wl);
     if ((st = upload_list(c, dev, s))) return st;
     WorkList wl{dev, dev + workers + 1, workers, units};
-    if ((st = tc_bwd_pipelined(p, q, k, v, dO, lse2, delta, L.Lq_pad, dq, dK_acc, dV_acc, true, &wl, s)))
+    if ((st = tc_bwd_pipelined(p, q, k, v, dO, nlse2, delta, L.Lq_pad, dq, dK_acc, dV_acc, true, &wl, s)))
         return st;
     count_launch(DFA_KERNEL_BWD);
     st = launch_convert(DFA_F32, B, H, Lq, D, scale, dq, dQ_acc, true, s);
@@ -623,7 +623,7 @@ int g_stage_next[kMaxDevices] = {};
 std::mutex g_stage_mu;
 
 struct VarlenLayout {
-    size_t delta = 0, lse2 = 0, dq = 0, seq = 0, wl = 0, total = 0;
+    size_t delta = 0, nlse2 = 0, dq = 0, seq = 0, wl = 0, total = 0;
     int64_t T = 0, P = 0;        // tokens; 128-row padded rows per head
     int units_max = 0;           // work units of the longest sequence
     int64_t items = 0;           // work items over all sequences and heads
@@ -659,7 +659,7 @@ bool varlen_layout(const int32_t* cu, int n, int H, int Hkv, int D, bool bwd, Va
     if (bwd) {
         L->delta = off;
         off = align_up(off + sizeof(float) * (size_t)H * L->P);
-        L->lse2 = off;
+        L->nlse2 = off;
         off = align_up(off + sizeof(float) * (size_t)H * L->P);
         L->dq = off;
         off = align_up(off + sizeof(float) * (size_t)H * L->P * D);
@@ -792,15 +792,15 @@ extern "C" dfa_status dfa_attn_bwd_varlen(const void* q, const void* k, const vo
     const int32_t* seq = reinterpret_cast<const int32_t*>(ws + L.seq);
     const int32_t* wl_dev = reinterpret_cast<const int32_t*>(ws + L.wl);
     float* delta = reinterpret_cast<float*>(ws + L.delta);
-    float* lse2 = reinterpret_cast<float*>(ws + L.lse2);
+    float* nlse2 = reinterpret_cast<float*>(ws + L.nlse2);
     float* dq_acc = reinterpret_cast<float*>(ws + L.dq);
-    if ((st = launch_bwd_prep_varlen(n_seq, H, L.T, L.P, D, seq, O, dO, lse, lse2, delta, s))) return st;
+    if ((st = launch_bwd_prep_varlen(n_seq, H, L.T, L.P, D, seq, O, dO, lse, nlse2, delta, s))) return st;
     count_launch(DFA_KERNEL_DELTA);
     cudaError_t e = cudaMemsetAsync(dq_acc, 0, sizeof(float) * (size_t)H * L.P * D, s);
     if (e != cudaSuccess) return fail(DFA_ERR_CUDA, "dQ accumulator clear: %s", cudaGetErrorString(e));
     const AttnProblem p = varlen_problem(n_seq, H, H_kv, L.T, D, causal, scale, seq);
     WorkList wl{wl_dev, wl_dev + workers + 1, workers, std::max(L.units_max, 1)};
-    if ((st = tc_bwd(p, q, k, v, dO, lse2, delta, (int)L.P, dq_acc, dK, dV, &wl, s))) return st;
+    if ((st = tc_bwd(p, q, k, v, dO, nlse2, delta, (int)L.P, dq_acc, dK, dV, &wl, s))) return st;
     count_launch(DFA_KERNEL_BWD);
     st = launch_convert_varlen(n_seq, H, L.T, L.P, D, scale, seq, dq_acc, dQ, s);
     if (st == DFA_OK) count_launch(DFA_KERNEL_CONVERT);

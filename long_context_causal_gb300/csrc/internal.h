@@ -25,7 +25,7 @@ struct AttnProblem {
     // Variable-length batch (device, int32): seq[0..B] are the first tokens of
     // the B sequences in the packed [1, Lq, heads, D] tensors (Lq = Lkv = T
     // tokens), seq[B+1..2B+1] their first rows in the 128-row-padded per-head
-    // arrays of the backward (lse2, Delta, fp32 dQ accumulator).  nullptr: dense.
+    // arrays of the backward (nlse2, Delta, fp32 dQ accumulator).  nullptr: dense.
     const int32_t* seq = nullptr;
 };
 
@@ -59,15 +59,16 @@ dfa_status launch_merge_pieces(dfa_dtype dt, int B, int H, int S, int D, int cau
 // Delta[b,h,i] = sum_d dO[b,i,h,d] * O[b,i,h,d]   (dense BSHD, fp32 out [B,H,S]).
 dfa_status launch_delta(dfa_dtype dt, int B, int H, int S, int D, const void* O,
                         const void* dO, float* delta, cudaStream_t s);
-// Backward preprocessing for the tensor-core path: lse2 = lse * log2(e) and
+// Backward preprocessing for the tensor-core path: nlse2 = -lse * log2(e) (negated so
+// that a score's base-2 exponent is one fused multiply-add, s c2 + nlse2) and
 // Delta = rowsum(dO * O), both written to [B, H, S_pad] with zero padding.
 dfa_status launch_bwd_prep(dfa_dtype dt, int B, int H, int S, int S_pad, int D, const void* O,
-                           const void* dO, const float* lse, float* lse2, float* delta, cudaStream_t s);
+                           const void* dO, const float* lse, float* nlse2, float* delta, cudaStream_t s);
 // Packed batch of n_seq sequences, T tokens, bf16 (seq as in AttnProblem::seq,
-// P = padded rows per head): lse2 and Delta [H, P] (zero past each sequence's
+// P = padded rows per head): nlse2 and Delta [H, P] (zero past each sequence's
 // end) from O, dO [T, H, D] and lse [H, T]; and dQ [T, H, D] = scale * acc [H, P, D].
 dfa_status launch_bwd_prep_varlen(int n_seq, int H, int64_t T, int64_t P, int D, const int32_t* seq,
-                                  const void* O, const void* dO, const float* lse, float* lse2, float* delta,
+                                  const void* O, const void* dO, const float* lse, float* nlse2, float* delta,
                                   cudaStream_t s);
 dfa_status launch_convert_varlen(int n_seq, int H, int64_t T, int64_t P, int D, float scale, const int32_t* seq,
                                  const float* acc, void* out, cudaStream_t s);
@@ -95,10 +96,10 @@ struct WorkList {
 // goes to O + s * B*Lq*H*D and lse + s * B*H*Lq.
 dfa_status tc_fwd(const AttnProblem& p, const void* q, const void* k, const void* v, void* O,
                   bool O_is_f32, float* lse, const WorkList* wl, cudaStream_t s);
-// lse2 = lse * log2(e) and delta are [B, H, S_pad] (S_pad = S rounded up to 128,
+// nlse2 = -lse * log2(e) and delta are [B, H, S_pad] (S_pad = S rounded up to 128,
 // zero in the padding); dq_acc is fp32 [B, S, H, D] and must be zero.
 dfa_status tc_bwd(const AttnProblem& p, const void* q, const void* k, const void* v,
-                  const void* dO, const float* lse2, const float* delta, int S_pad, float* dq_acc,
+                  const void* dO, const float* nlse2, const float* delta, int S_pad, float* dq_acc,
                   void* dK, void* dV, const WorkList* wl, cudaStream_t s);
 
 // Head-dim-128 backward with the softmax-gradient split into two phases so the
@@ -106,7 +107,7 @@ dfa_status tc_bwd(const AttnProblem& p, const void* q, const void* k, const void
 // Problems with Lq != Lkv and offsets (kv_offset - q_offset a multiple of 128)
 // are the chunk-pair backward; acc_f32 makes dK/dV fp32 accumulators (+=).
 dfa_status tc_bwd_pipelined(const AttnProblem& p, const void* q, const void* k, const void* v,
-                            const void* dO, const float* lse2, const float* delta, int S_pad,
+                            const void* dO, const float* nlse2, const float* delta, int S_pad,
                             float* dq_acc, void* dK, void* dV, bool acc_f32, const WorkList* wl,
                             cudaStream_t s);
 

@@ -426,6 +426,25 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return r;
 }
 
+// Two probabilities packed to bf16x2, `lo` = 2^(s0 c + n0) and `hi` =
+// 2^(s1 c + n1): both exponents from one two-lane fused multiply-add
+// (fma.f32x2, each lane rounded as fmaf), then the hardware exp2 as ex2().
+__device__ __forceinline__ uint32_t exp2_pack_bf16(float s0, float s1, float c, float n0, float n1) {
+    uint32_t r;
+    asm("{\n\t.reg .b64 a, b, d;\n\t.reg .f32 lo, hi;\n\t"
+        "mov.b64 a, {%1, %2};\n\t"
+        "mov.b64 b, {%3, %3};\n\t"
+        "mov.b64 d, {%4, %5};\n\t"
+        "fma.rn.f32x2 a, a, b, d;\n\t"
+        "mov.b64 {lo, hi}, a;\n\t"
+        "ex2.approx.ftz.f32 lo, lo;\n\t"
+        "ex2.approx.ftz.f32 hi, hi;\n\t"
+        "cvt.rn.bf16x2.f32 %0, hi, lo;\n\t}"
+        : "=r"(r)
+        : "f"(s0), "f"(s1), "f"(c), "f"(n0), "f"(n1));
+    return r;
+}
+
 // Two softmax-gradient entries packed to bf16x2, `lo` = p0 (u0 - d0) and
 // `hi` = p1 (u1 - d1), with the two-lane fp32 instructions of sm_100 and later
 // (sub.f32x2, mul.f32x2): each lane is rounded exactly as the scalar
