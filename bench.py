@@ -55,7 +55,7 @@ def parse():
 # single-pass ncu capture of this command's workload (profiles/
 # launches_llama7b_s128k.md).  Only valid for the kernel build it was taken on;
 # other workloads report null.
-NCU_BWD_TRAFFIC = {"llama7b_s128k": 243.38e9}
+NCU_BWD_TRAFFIC = {"llama7b_s128k": 92.92e9}
 
 
 def measured_peaks():
