@@ -44,7 +44,7 @@ extern "C" {
 typedef enum {
     DFA_OK = 0,
     DFA_ERR_INVALID_ARG = 1,   /* bad pointer, size, stride, alignment or scale   */
-    DFA_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement     */
+    DFA_ERR_UNSUPPORTED = 2,   /* valid request the library does not implement   */
     DFA_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed            */
     DFA_ERR_TIMEOUT = 4,       /* a kernel gave up on a bounded wait              */
     DFA_ERR_WORKSPACE = 5      /* workspace missing or smaller than required      */
