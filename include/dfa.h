@@ -141,7 +141,8 @@ size_t dfa_chunk_bwd_workspace_size(int B, int H, int H_kv, int Lq, int Lkv, int
 /* Bytes of workspace dfa_attn_fwd (bwd = 0) or dfa_attn_bwd (bwd = 1) needs,
  * for every schedule: on a problem small enough for SPLIT_KV it includes the
  * pieces' fp32 partials (forward) or dK/dV accumulators (backward), sized
- * for the current device's SM count.  Returns 0 for invalid sizes. */
+ * for the current device's SM count.  Returns 0 for invalid sizes, including
+ * an n_chunks that leaves the last chunk empty. */
 size_t dfa_attn_workspace_size(int B, int H, int H_kv, int S, int D, int n_chunks, int bwd);
 
 /* Whole-sequence causal forward over n_chunks token chunks (DISTFLASHATTN §3.1,
@@ -149,7 +150,11 @@ size_t dfa_attn_workspace_size(int B, int H, int H_kv, int S, int D, int n_chunk
  * rescale-and-merge rule as the key/value chunks stream by, so the result
  * equals the monolithic softmax up to rounding.
  *   q: [B, S, H, D], k, v: [B, S, H_kv, D] dense;  O: [B, S, H, D] in dt;
- *   lse: fp32 [B, H, S] (saved for the backward).  S % n_chunks == 0. */
+ *   lse: fp32 [B, H, S] (saved for the backward).
+ * Chunks: the first n_chunks - 1 hold C = ceil(S / n_chunks) tokens and the
+ * last one the rest (a ragged last chunk), which must hold at least one
+ * token, else INVALID_ARG (e.g. S = 9, n_chunks = 4).  n_chunks changes only
+ * the decomposition, never the result. */
 dfa_status dfa_attn_fwd(const void* q, const void* k, const void* v, dfa_dtype dt,
                         int B, int H, int H_kv, int S, int D, int n_chunks, int causal,
                         float scale, dfa_sched sched, void* O, float* lse,
@@ -176,7 +181,8 @@ dfa_status dfa_attn_bwd(const void* q, const void* k, const void* v, const void*
  * attends only to its own chunk and the neighbouring chunks before it, and
  * fetches only those key/value blocks).  Causal attention in which a query at
  * position qp sees key kp only if kp <= qp and kp / C >= qp / C - (window - 1),
- * C = S / n_chunks the chunk length; window >= n_chunks is plain causal.
+ * C = ceil(S / n_chunks) the chunk length (the last chunk may be shorter);
+ * window >= n_chunks is plain causal.
  * Arguments, layouts, workspace and errors as dfa_attn_fwd / dfa_attn_bwd
  * (causal implied); INVALID_ARG for window < 1.  Key/value tiles entirely
  * outside a query tile's window are not loaded or computed. */

@@ -271,7 +271,7 @@ extern "C" int64_t dfa_launch_count(dfa_kernel_kind kind) {
 
 extern "C" size_t dfa_attn_workspace_size(int B, int H, int H_kv, int S, int D, int n_chunks, int bwd) {
     if (B < 0 || H <= 0 || H_kv <= 0 || S < 0 || n_chunks <= 0 || (D != 64 && D != 128)) return 0;
-    if (H % H_kv != 0 || (S % n_chunks) != 0) return 0;
+    if (H % H_kv != 0 || !chunks_valid(S, n_chunks)) return 0;
     return layout(B, H, H_kv, S, D, bwd != 0).total;
 }
 
@@ -332,8 +332,9 @@ static dfa_status check_whole(dfa_dtype dt, int B, int H, int H_kv, int S, int D
     dfa_status st;
     if ((st = check_dtype(dt)) || (st = check_common(B, H, H_kv, D, scale))) return st;
     if (S < 0) return fail(DFA_ERR_INVALID_ARG, "negative sequence length");
-    if (n_chunks <= 0 || S % n_chunks != 0)
-        return fail(DFA_ERR_INVALID_ARG, "S=%d must split into n_chunks=%d equal chunks", S, n_chunks);
+    if (!chunks_valid(S, n_chunks))
+        return fail(DFA_ERR_INVALID_ARG, "S=%d does not split into n_chunks=%d non-empty chunks of ceil(S/n_chunks) tokens",
+                    S, n_chunks);
     if (sched != DFA_SCHED_BALANCED && sched != DFA_SCHED_UNBALANCED && sched != DFA_SCHED_SPLIT_KV)
         return fail(DFA_ERR_INVALID_ARG, "unknown schedule %d", (int)sched);
     if ((int64_t)B * S == 0) return DFA_OK;
@@ -348,7 +349,7 @@ static AttnProblem whole_problem(int B, int H, int H_kv, int S, int D, int causa
                                  int n_chunks = 1, int window = 0) {
     AttnProblem p{};
     if (window > 0) {
-        p.win_c = S / n_chunks;
+        p.win_c = chunk_tokens(S, n_chunks);   // the last chunk may be shorter
         p.win_w = window;
     }
     p.B = B; p.H = H; p.Hkv = H_kv; p.Lq = S; p.Lkv = S; p.D = D;

@@ -113,6 +113,15 @@ dfa_status tc_bwd_pipelined(const AttnProblem& p, const void* q, const void* k, 
 
 int num_sms();
 
+// A sequence of S tokens cut into n_chunks chunks (DISTFLASHATTN §3.1: one
+// chunk per worker): every chunk but the last holds ceil(S / n_chunks)
+// tokens and the last one the rest, which must be at least one token.  An
+// empty sequence splits into any positive number of chunks.
+inline int64_t chunk_tokens(int64_t S, int n_chunks) { return (S + n_chunks - 1) / n_chunks; }
+inline bool chunks_valid(int64_t S, int n_chunks) {
+    return n_chunks > 0 && (S == 0 || (int64_t)(n_chunks - 1) * chunk_tokens(S, n_chunks) < S);
+}
+
 // 4-D bf16 TMA descriptor over a [B, L, heads, D] tensor (element strides sb,
 // ss, sh; D contiguous), box {64, 1, 128, 1}, 128-byte swizzle.  The map is
 // written into `map` (a CUtensorMap, 128 bytes, 64-byte aligned).

@@ -112,8 +112,9 @@ extern "C" dfa_status dfa_attn_fwd_noalloc(const void* q, const void* k, const v
     if (H % H_kv != 0) return fail(DFA_ERR_INVALID_ARG, "H (%d) must be a multiple of H_kv (%d)", H, H_kv);
     if (D != 64 && D != 128) return fail(DFA_ERR_UNSUPPORTED, "head dim D=%d (supported: 64, 128)", D);
     if (!(scale > 0.f) || !std::isfinite(scale)) return fail(DFA_ERR_INVALID_ARG, "scale must be finite and > 0");
-    if (n_chunks <= 0 || S % n_chunks != 0)
-        return fail(DFA_ERR_INVALID_ARG, "S=%d must split into n_chunks=%d equal chunks", S, n_chunks);
+    if (!chunks_valid(S, n_chunks))
+        return fail(DFA_ERR_INVALID_ARG, "S=%d does not split into n_chunks=%d non-empty chunks of ceil(S/n_chunks) tokens",
+                    S, n_chunks);
     if (sched != DFA_SCHED_BALANCED && sched != DFA_SCHED_UNBALANCED && sched != DFA_SCHED_SPLIT_KV)
         return fail(DFA_ERR_INVALID_ARG, "unknown schedule %d", (int)sched);
     if (sched == DFA_SCHED_SPLIT_KV) sched = DFA_SCHED_BALANCED;   // no workspace for pieces

@@ -328,8 +328,9 @@ def dfa_attn_bwd(q, k, v, O, lse, dO, n_chunks: int = 1, causal: bool = True,
 
 def dfa_attn_fwd_local(q, k, v, n_chunks: int, window: int, scale: float | None = None, sched="balanced",
                        O=None, lse=None, workspace_buf=None, stream=None):
-    """Causal forward restricted to a local window of `window` chunks (S / n_chunks
-    tokens each): returns (O, lse) like dfa_attn_fwd."""
+    """Causal forward restricted to a local window of `window` chunks
+    (ceil(S / n_chunks) tokens each, the last chunk possibly shorter): returns
+    (O, lse) like dfa_attn_fwd."""
     B, S, H, D = q.shape
     Hkv = k.shape[2]
     for t, n in ((q, "q"), (k, "k"), (v, "v")):

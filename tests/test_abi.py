@@ -57,8 +57,11 @@ def test_whole_sequence_validation():
     f = lib.dfa_attn_fwd
     ws = dfa.dfa_attn_workspace_size(1, 4, 2, 1024, 128, 4, 0)
     assert ws > 0 and ws % 256 == 0
-    # S not divisible by n_chunks
-    assert f(A, A, A, 1, 1, 4, 2, 1000, 128, 3, 1, 0.1, 0, A, A, A, ws, None) == dfa.DFA_ERR_INVALID_ARG
+    # n_chunks that leaves the last chunk empty (S = 9: chunks of 3, 3, 3 and 0); a
+    # ragged last chunk is valid (S = 1000, 3 chunks of 334, 334, 332)
+    assert f(A, A, A, 1, 1, 4, 2, 9, 128, 4, 1, 0.1, 0, A, A, A, ws, None) == dfa.DFA_ERR_INVALID_ARG
+    assert f(A, A, A, 1, 1, 4, 2, 8, 128, 9, 1, 0.1, 0, A, A, A, ws, None) == dfa.DFA_ERR_INVALID_ARG
+    assert dfa.dfa_attn_workspace_size(1, 4, 2, 1000, 128, 3, 0) > 0
     # workspace too small / missing
     assert f(A, A, A, 1, 1, 4, 2, 1024, 128, 4, 1, 0.1, 0, A, A, A, ws - 256, None) == dfa.DFA_ERR_WORKSPACE
     assert f(A, A, A, 1, 1, 4, 2, 1024, 128, 4, 1, 0.1, 0, A, A, None, ws, None) == dfa.DFA_ERR_WORKSPACE
@@ -75,7 +78,8 @@ def test_whole_sequence_validation():
 
 def test_workspace_size_rejects_bad_shapes():
     assert dfa.dfa_attn_workspace_size(1, 3, 2, 128, 128, 1, 0) == 0
-    assert dfa.dfa_attn_workspace_size(1, 4, 2, 100, 128, 3, 0) == 0
+    assert dfa.dfa_attn_workspace_size(1, 4, 2, 9, 128, 4, 0) == 0
+    assert dfa.dfa_attn_workspace_size(1, 4, 2, 100, 128, 0, 0) == 0
     assert dfa.dfa_attn_workspace_size(1, 4, 2, 128, 80, 1, 1) == 0
 
 

@@ -3,8 +3,8 @@ fp64 oracle: a query sees its own chunk and the window - 1 chunks before it.
 
 Cases cover chunk lengths that are multiples of the 256-row forward block, of
 the 128-row tile only (a block straddles two windows), and of neither (the
-window edge cuts through tiles), head dims 128 and 64, GQA, and fp32 on the
-CUDA-core kernels.  Tolerances as in the other parity tests.
+window edge cuts through tiles), a ragged last chunk (S not a multiple of
+n_chunks), head dims 128 and 64, GQA, and fp32 on the CUDA-core kernels.  Tolerances as in the other parity tests.
 """
 import numpy as np
 import pytest
@@ -46,6 +46,10 @@ CASES = [
     (2, 2, 1, 1024, 128, torch.bfloat16, 8, 3, "C=128, three chunks, batch 2"),
     (1, 2, 2, 768, 64, torch.bfloat16, 3, 2, "D=64"),
     (1, 2, 1, 300, 64, torch.float32, 3, 2, "fp32 on CUDA cores"),
+    (1, 4, 2, 1000, 128, torch.bfloat16, 3, 2, "ragged last chunk: 334, 334, 332"),
+    (1, 2, 1, 2301, 128, torch.bfloat16, 5, 2, "ragged last chunk: four of 461, one of 457"),
+    (1, 2, 2, 700, 64, torch.bfloat16, 3, 1, "ragged last chunk, D=64: 234, 234, 232"),
+    (1, 2, 1, 301, 64, torch.float32, 4, 2, "ragged last chunk, fp32: 76, 76, 76, 73"),
 ]
 
 
@@ -56,7 +60,7 @@ def test_local_window_matches_oracle(case):
     O, lse = dfa.dfa_attn_fwd_local(q, k, v, n_chunks=P, window=w)
     grads = dfa.dfa_attn_bwd_local(q, k, v, O, lse, do, n_chunks=P, window=w)
     dfa.dfa_check_errors()
-    C = S // P
+    C = -(-S // P)   # every chunk but the last holds ceil(S / P) tokens
     Or, lr = oracle.attn_fwd_local(np64(q), np64(k), np64(v), chunk=C, window=w)
     refs = oracle.attn_bwd_local(np64(q), np64(k), np64(v), np64(do), chunk=C, window=w)
     check(O, lse, grads, Or, lr, refs, dtype, what)

@@ -269,6 +269,30 @@ def test_window_gradients_match_finite_differences():
         assert np.max(np.abs(fd - g) / np.maximum(1.0, np.abs(g))) < 1e-7, idx
 
 
+@pytest.mark.parametrize("S,C,w", [(14, 4, 1), (14, 4, 2), (11, 3, 3), (9, 5, 1)])
+def test_window_with_a_ragged_last_chunk_matches_torch_sdpa(S, C, w):
+    # chunks of C tokens and a shorter last one (S = 14, C = 4: 4, 4, 4, 2);
+    # the window mask written from its definition, attention by torch in fp64
+    B, H, Hkv, D, scale = 1, 2, 1, 5, 0.6
+    q, k, v, dO = rnd((B, S, H, D), 440), rnd((B, S, Hkv, D), 441), rnd((B, S, Hkv, D), 442), rnd((B, S, H, D), 443)
+    O, lse = oracle.attn_fwd_local(q, k, v, chunk=C, window=w, scale=scale)
+    dQ, dK, dV = oracle.attn_bwd_local(q, k, v, dO, chunk=C, window=w, scale=scale)
+    i, j = np.arange(S)[:, None], np.arange(S)[None, :]
+    allow = torch.tensor((j <= i) & (j // C >= i // C - (w - 1)))
+    tq = torch.tensor(q).transpose(1, 2).requires_grad_()
+    tk = torch.tensor(k).transpose(1, 2).requires_grad_()
+    tv = torch.tensor(v).transpose(1, 2).requires_grad_()
+    kk, vv = tk.repeat_interleave(H // Hkv, dim=1), tv.repeat_interleave(H // Hkv, dim=1)
+    out = torch.nn.functional.scaled_dot_product_attention(tq, kk, vv, attn_mask=allow, scale=scale)
+    out.backward(torch.tensor(dO).transpose(1, 2))
+    np.testing.assert_allclose(O, out.detach().transpose(1, 2).numpy(), atol=1e-12)
+    np.testing.assert_allclose(dQ, tq.grad.transpose(1, 2).numpy(), atol=1e-11)
+    np.testing.assert_allclose(dK, tk.grad.transpose(1, 2).numpy(), atol=1e-11)
+    np.testing.assert_allclose(dV, tv.grad.transpose(1, 2).numpy(), atol=1e-11)
+    s = scale * torch.einsum("bhid,bhjd->bhij", tq.detach(), kk.detach()).masked_fill(~allow, float("-inf"))
+    np.testing.assert_allclose(lse, torch.logsumexp(s, dim=-1).numpy(), atol=1e-12)
+
+
 def test_merge_neutral_element_and_symmetry():
     O_a, O_b = rnd((1, 3, 2, 4), 80), rnd((1, 3, 2, 4), 81)
     la, lb = rnd((1, 2, 3), 82), rnd((1, 2, 3), 83)

@@ -145,8 +145,8 @@ def test_merge_matches_oracle_including_empty_rows():
 
 @pytest.mark.parametrize("shape", [(1, 5, 3, 64), (1, 7, 2, 12), (2, 3, 1, 1032), (3, 333, 5, 128)])
 def test_merge_row_groups_ragged_and_in_place(shape):
-    # Warps take groups of rows (several short rows, or chunks of one long
-    # row); the last group is ragged, and the output may alias either input.
+    # Rows shorter and longer than a warp's 128 floats, odd row counts, and
+    # the output aliasing either input.
     B, L, H, D = shape
     g = torch.Generator(device=DEV).manual_seed(13)
     Oa = torch.randn((B, L, H, D), generator=g, device=DEV)
@@ -224,6 +224,23 @@ def test_backward_reuses_saved_outputs_and_never_runs_the_forward():
     dfa.dfa_attn_bwd(q, k, v, O1, l1, do, n_chunks=3)
     dfa.dfa_check_errors()
     assert dfa.dfa_launch_count("fwd") == before
+
+
+def test_ragged_last_chunk_changes_only_the_decomposition():
+    # S = 1000 in 3 chunks (334, 334, 332) and in 7 (143 x 6, 142): n_chunks
+    # never changes the result, so the bits equal those of one chunk.
+    q, k, v, do = make(1, 4, 2, 1000, 128, torch.bfloat16, seed=19, device=DEV)
+    O1, l1 = dfa.dfa_attn_fwd(q, k, v, n_chunks=1)
+    g1 = dfa.dfa_attn_bwd(q, k, v, O1, l1, do, n_chunks=1)
+    for P in (3, 7):
+        O, l = dfa.dfa_attn_fwd(q, k, v, n_chunks=P)
+        g = dfa.dfa_attn_bwd(q, k, v, O, l, do, n_chunks=P)
+        dfa.dfa_check_errors()
+        assert torch.equal(O, O1) and torch.equal(l, l1), P
+        assert torch.equal(g[1], g1[1]) and torch.equal(g[2], g1[2]), P
+    with pytest.raises(dfa.DfaError) as e:   # S = 9 in 4 chunks of 3 leaves the last one empty
+        dfa.dfa_attn_fwd(q[:, :9].contiguous(), k[:, :9].contiguous(), v[:, :9].contiguous(), n_chunks=4)
+    assert e.value.status == dfa.DFA_ERR_INVALID_ARG
 
 
 def test_schedules_give_the_same_forward_bits():
