@@ -47,15 +47,38 @@ def parse():
     ap.add_argument("--window", type=int, default=2, help="chunks per local window for the extra local-window timing (0: skip)")
     ap.add_argument("--no-varlen", action="store_true", help="skip the packed-batch timing")
     ap.add_argument("--no-split-kv", action="store_true", help="skip the small-problem split-kv forward timing")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target oracle sample time")
+    ap.add_argument("--cpu-seconds", type=float, default=8.0, help="target oracle sample time")
+    ap.add_argument("--no-unbalanced", action="store_true", help="skip the unbalanced work-list timing")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the timing of the other Llama-7B workloads (32K, GQA 64K, 512K)")
     return ap.parse_args()
 
 
-# DRAM bytes (read + write) per launch of the backward kernel, from one
-# single-pass ncu capture of this command's workload (profiles/
-# launches_llama7b_s128k.md).  Only valid for the kernel build it was taken on;
-# other workloads report null.
-NCU_BWD_TRAFFIC = {"llama7b_s128k": 92.92e9}
+# DRAM bytes (read + write) of one launch of the backward kernel, measured by
+# ncu on one launch of the 32K Llama-7B workload (one kernel, one launch, a few
+# GB on the device), and the forward kernel's the same way.  A larger workload
+# of the same head shape is scaled by its ratio of causal (query, key) pairs:
+# an estimate, because how much of the fp32 dQ accumulator stays in L2 changes
+# with the size.  Valid only for the kernel builds they were taken on.
+NCU_TRAFFIC_REF = {"workload": "llama7b_s32k", "bwd": None, "fwd": None}
+
+
+def config_of(w, sched):
+    """The `config` object of both arms' JSON lines (the same for the same workload)."""
+    return {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.H_kv, "S": w.S, "D": w.D,
+            "n_chunks": w.n_chunks, "sched": sched, "causal": True,
+            "l2": "inputs larger than L2 (each tensor exceeds 129 MB)"}
+
+
+def scaled_traffic(w, kernel):
+    """DRAM bytes per launch of `kernel` ("bwd" or "fwd") for workload w, scaled
+    from the single-launch capture of NCU_TRAFFIC_REF, or None."""
+    from long_context_causal_gb300.inputs import WORKLOADS
+    measured = NCU_TRAFFIC_REF[kernel]
+    ref = WORKLOADS[NCU_TRAFFIC_REF["workload"]]
+    if measured is None or w.D != ref.D or w.H // w.H_kv != ref.H // ref.H_kv:
+        return None
+    return measured * w.causal_flops() / ref.causal_flops()
 
 
 def measured_peaks():
@@ -216,8 +239,7 @@ def run_reference(args, w):
         "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.H_kv, "S": w.S, "D": w.D,
-                   "n_chunks": w.n_chunks},
+        "config": config_of(w, args.sched),
         "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc},
         "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -233,17 +255,19 @@ def chunk_step_timing(w, q, k, v, O, lse, do, stream, dfa, reps=5):
     import torch
     if w.n_chunks < 2:
         return None
-    C = w.S // w.n_chunks
+    C = -(-w.S // w.n_chunks)     # the library's chunk length: ceil(S / n_chunks), the last chunk shorter
     out = {"C": C}
     f32 = dict(dtype=torch.float32, device=q.device)
-    ws = torch.empty(max(dfa.dfa_chunk_bwd_workspace_size(w.B, w.H, w.H_kv, C, C, w.D), 16),
+    ws = torch.empty(max(dfa.dfa_chunk_bwd_workspace_size(w.B, w.H, w.H_kv, Cq, C, w.D), 16),
                      dtype=torch.uint8, device=q.device)
-    Op = torch.empty((w.B, C, w.H, w.D), **f32)
-    lp = torch.empty((w.B, w.H, C), **f32)
-    acc = (torch.zeros((w.B, C, w.H, w.D), **f32), torch.zeros((w.B, C, w.H_kv, w.D), **f32),
+    Op = torch.empty((w.B, Cq, w.H, w.D), **f32)
+    lp = torch.empty((w.B, w.H, Cq), **f32)
+    acc = (torch.zeros((w.B, Cq, w.H, w.D), **f32), torch.zeros((w.B, C, w.H_kv, w.D), **f32),
            torch.zeros((w.B, C, w.H_kv, w.D), **f32))
-    for name, (qa, ka) in (("off_diagonal", (w.S - C, 0)), ("diagonal", (w.S - C, w.S - C))):
-        qs, ks = slice(qa, qa + C), slice(ka, ka + C)
+    last = (w.n_chunks - 1) * C   # first token of the last chunk
+    Cq = w.S - last
+    for name, (qa, ka, Lk) in (("off_diagonal", (last, 0, C)), ("diagonal", (last, last, Cq))):
+        qs, ks = slice(qa, qa + Cq), slice(ka, ka + Lk)
         qc, kc, vc, dc = (t.contiguous() for t in (q[:, qs], k[:, ks], v[:, ks], do[:, qs]))
         Oc, lc = O[:, qs].contiguous(), lse[:, :, qs].contiguous()
 
@@ -253,7 +277,8 @@ def chunk_step_timing(w, q, k, v, O, lse, do, stream, dfa, reps=5):
 
         def bwd():
             dfa.dfa_chunk_attn_bwd(qc, kc, vc, Oc, lc, dc, q_offset=qa, kv_offset=ka, scale=w.scale,
-                                   dQ_acc=acc[0], dK_acc=acc[1], dV_acc=acc[2], workspace_buf=ws, stream=stream)
+                                   dQ_acc=acc[0], dK_acc=acc[1][:, :Lk], dV_acc=acc[2][:, :Lk], workspace_buf=ws,
+                                   stream=stream)
 
         res = {}
         for tag, fn, per_pair in (("fwd", fwd, 4), ("bwd", bwd, 10)):
@@ -267,7 +292,7 @@ def chunk_step_timing(w, q, k, v, O, lse, do, stream, dfa, reps=5):
             b.record(stream)
             torch.cuda.synchronize(q.device)
             ms = a.elapsed_time(b) / reps
-            pairs = w.B * w.H * (C * C if qa != ka else C * (C + 1) // 2)
+            pairs = w.B * w.H * (Cq * Lk if qa != ka else Cq * (Cq + 1) // 2)
             res[f"{tag}_ms"] = ms
             res[f"{tag}_tflops"] = pairs * w.D * per_pair / (ms * 1e-3) / 1e12
         out[name] = res
@@ -314,7 +339,7 @@ def local_window_timing(w, window, q, k, v, do, stream, dfa, reps=3):
     import torch
     if w.n_chunks < 2 or window >= w.n_chunks:
         return None
-    C = w.S // w.n_chunks
+    C = -(-w.S // w.n_chunks)     # the library's chunk length: ceil(S / n_chunks)
     O = torch.empty_like(q)
     lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=q.device)
     dQ, dK, dV = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
@@ -458,6 +483,134 @@ def varlen_timing(device, stream, dfa, H=32, Hkv=32, D=128, reps=3):
     return out
 
 
+def timed_ms(fn, device, stream, reps, warm=1):
+    """Mean device time of fn() over reps calls (CUDA events on `stream`)."""
+    import torch
+    for _ in range(warm):
+        fn()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(device)
+    a.record(stream)
+    for _ in range(reps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize(device)
+    return a.elapsed_time(b) / reps
+
+
+def fwd_bwd_legs(w, q, k, v, do, O, lse, dQ, dK, dV, wsf, wsb, sched, stream, dfa, reps, warm):
+    """fwd, bwd and fwd + bwd ms and TFLOP/s of one workload under one schedule."""
+    def fwd():
+        dfa.dfa_attn_fwd(q, k, v, n_chunks=w.n_chunks, scale=w.scale, sched=sched, O=O, lse=lse,
+                         workspace_buf=wsf, stream=stream)
+
+    def bwd():
+        dfa.dfa_attn_bwd(q, k, v, O, lse, do, n_chunks=w.n_chunks, scale=w.scale, sched=sched,
+                         dQ=dQ, dK=dK, dV=dV, workspace_buf=wsb, stream=stream)
+    f_ms = timed_ms(fwd, q.device, stream, reps, warm)
+    b_ms = timed_ms(bwd, q.device, stream, reps, warm)
+    dfa.dfa_check_errors(stream)
+    ff, bf = w.causal_flops(True, False), w.causal_flops(False, True)
+    return {"fwd_ms": f_ms, "bwd_ms": b_ms, "total_ms": f_ms + b_ms,
+            "fwd_tflops": ff / (f_ms * 1e-3) / 1e12, "bwd_tflops": bf / (b_ms * 1e-3) / 1e12,
+            "tflops": (ff + bf) / ((f_ms + b_ms) * 1e-3) / 1e12,
+            "pct_of_nominal_bf16_peak": 100.0 * (ff + bf) / ((f_ms + b_ms) * 1e-3) / 1e12 / NOMINAL_BF16_TFLOPS}
+
+
+def unbalanced_timing(w, tensors, stream, dfa, balanced, reps=3):
+    """The same workload with the unbalanced work list (each persistent CTA
+    takes one contiguous token range per head, the pages' baseline
+    distribution of the causal triangle, DISTFLASHATTN §4.5 / Fig. 4) against
+    the balanced list of the headline."""
+    out = fwd_bwd_legs(w, *tensors, "unbalanced", stream, dfa, reps, 1)
+    out["balanced_over_unbalanced"] = out["total_ms"] / balanced["total_ms"]
+    out["balanced"] = balanced
+    return out
+
+
+OTHER_WORKLOADS = ("llama7b_s32k", "llama7b_gqa8_s64k", "llama7b_s512k")
+
+
+def workloads_timing(device, stream, dfa, names=OTHER_WORKLOADS):
+    """fwd / bwd / fwd + bwd of the other Llama-7B workloads (32K, GQA 32/8
+    heads at 64K with K x 2, 512K), balanced list, each on its own inputs
+    (freed before the next).  The 512K step takes about 8 s: one warm-up step
+    and one timed step there, three elsewhere."""
+    import torch
+    from long_context_causal_gb300.inputs import WORKLOADS, make_workload
+    out = {}
+    for name in names:
+        w = WORKLOADS[name]
+        q, k, v, do = make_workload(w, device)
+        O, lse = torch.empty_like(q), torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=device)
+        dQ, dK, dV = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        wsf = dfa.workspace(w.B, w.H, w.H_kv, w.S, w.D, w.n_chunks, False, device)
+        wsb = dfa.workspace(w.B, w.H, w.H_kv, w.S, w.D, w.n_chunks, True, device)
+        reps = 1 if w.S >= 262144 else 3
+        r = fwd_bwd_legs(w, q, k, v, do, O, lse, dQ, dK, dV, wsf, wsb, "balanced", stream, dfa, reps, 1)
+        r.update({"B": w.B, "H": w.H, "H_kv": w.H_kv, "S": w.S, "D": w.D, "n_chunks": w.n_chunks, "reps": reps})
+        out[name] = r
+        del q, k, v, do, O, lse, dQ, dK, dV, wsf, wsb
+        torch.cuda.empty_cache()
+    return out
+
+
+def gpu_numa_cpus(index):
+    """(NUMA node, its CPU list) of GPU `index` from sysfs, or (None, None)."""
+    try:
+        bus = subprocess.run(["nvidia-smi", f"--id={index}", "--query-gpu=pci.bus_id", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=20).stdout.strip().lower()
+        # nvidia-smi prints an 8-digit PCI domain; sysfs uses 4 digits
+        dom, rest = bus.split(":", 1)
+        path = f"/sys/bus/pci/devices/{dom[-4:]}:{rest}/numa_node"
+        node = int(open(path).read().strip())
+        if node < 0:
+            return None, None
+        cpus = set()
+        for part in open(f"/sys/devices/system/node/node{node}/cpulist").read().strip().split(","):
+            a, _, b = part.partition("-")
+            cpus.update(range(int(a), int(b or a) + 1))
+        return node, sorted(cpus)
+    except Exception:
+        return None, None
+
+
+def copy_bandwidth(hin, xin, hout, yout, s_in, s_out, device, reps=3):
+    """GB/s of the step's host-to-device copies alone, of its device-to-host
+    copies alone, and of both at once, on the same pinned buffers and streams
+    as the end-to-end leg."""
+    import torch
+
+    def run(h2d, d2h):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        cur = torch.cuda.current_stream(device)
+        torch.cuda.synchronize(device)
+        a.record(cur)
+        s_in.wait_stream(cur)
+        s_out.wait_stream(cur)
+        for _ in range(reps):
+            if h2d:
+                with torch.cuda.stream(s_in):
+                    for d_, h_ in zip(xin, hin):
+                        d_.copy_(h_, non_blocking=True)
+            if d2h:
+                with torch.cuda.stream(s_out):
+                    for h_, d_ in zip(hout, yout):
+                        h_.copy_(d_, non_blocking=True)
+        cur.wait_stream(s_in)
+        cur.wait_stream(s_out)
+        b.record(cur)
+        torch.cuda.synchronize(device)
+        return a.elapsed_time(b) / reps
+    bi = sum(t.numel() * t.element_size() for t in hin)
+    bo = sum(t.numel() * t.element_size() for t in hout)
+    run(True, True)
+    t_in, t_out, t_both = run(True, False), run(False, True), run(True, True)
+    return {"h2d_gbs": bi / (t_in * 1e-3) / 1e9, "d2h_gbs": bo / (t_out * 1e-3) / 1e9,
+            "h2d_ms": t_in, "d2h_ms": t_out, "both_ms": t_both,
+            "both_gbs": (bi + bo) / (t_both * 1e-3) / 1e9}
+
+
 # ---------------------------------------------------------------- GPU arm
 def main():
     args = parse()
@@ -545,8 +698,22 @@ def main():
     # reuse of each buffer), as a training loop streaming its batches would run.
     e2e = None
     if not args.no_e2e:
-        hin = [t.cpu().pin_memory() for t in (q, k, v, do)]
-        hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (O, lse, dQ, dK, dV)]
+        # Pinned host buffers on the GPU's own NUMA node: pages are placed when
+        # they are pinned, on the node of the CPU that pins them, so the
+        # allocating thread runs on that node's CPUs meanwhile (no GPU setting
+        # is touched; the previous CPU affinity is restored).
+        node, cpus = gpu_numa_cpus(local if world > 1 else 0)
+        old_aff = os.sched_getaffinity(0)
+        if cpus:
+            try:
+                os.sched_setaffinity(0, cpus)
+            except OSError:
+                node = None
+        try:
+            hin = [t.cpu().pin_memory() for t in (q, k, v, do)]
+            hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (O, lse, dQ, dK, dV)]
+        finally:
+            os.sched_setaffinity(0, old_aff)
         h2d = sum(t.numel() * t.element_size() for t in hin)
         d2h = sum(t.numel() * t.element_size() for t in hout)
         xin = [(q, k, v, do), tuple(torch.empty_like(t) for t in (q, k, v, do))]
@@ -611,20 +778,38 @@ def main():
         barrier(world)
         dfa.dfa_check_errors(stream)
         e2e_ms = max_over_ranks(a.elapsed_time(b), world) / n_e2e
+        bw = copy_bandwidth(hin, xin[1], hout, yout[1], s_in, s_out, dev)
         e2e = {"value": job_value(flops, e2e_ms, world), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": n_e2e,
-               "copies": "overlapped with the neighbouring steps' compute on two copy streams"}
+               "copies": "overlapped with the neighbouring steps' compute on two copy streams",
+               "pinned_numa_node": node, **bw,
+               # a step costs at least max(compute, copies); the copies bound it when they take longer
+               "link_bound": bw["both_ms"] > ms_step}
         del xin, yout
 
+    balanced = {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "total_ms": fwd_ms + bwd_ms, "tflops": flops / ((fwd_ms + bwd_ms) * 1e-3) / 1e12}
+    unbal = None
+    if not args.no_unbalanced and args.sched == "balanced":
+        unbal = unbalanced_timing(w, (q, k, v, do, O, lse, dQ, dK, dV, wsf, wsb), stream, dfa, balanced)
     chunk = None if args.no_chunk_step else chunk_step_timing(w, q, k, v, O, lse, do, stream, dfa)
-    local = None if args.window <= 0 else local_window_timing(w, args.window, q, k, v, do, stream, dfa)
+    local_win = None if args.window <= 0 else local_window_timing(w, args.window, q, k, v, do, stream, dfa)
     split = None if args.no_split_kv else split_kv_timing(q.device, stream, dfa)
     varlen = None if args.no_varlen else varlen_timing(q.device, stream, dfa)
+    others = None
+    if not args.no_workloads and args.shape is None and w.name == "llama7b_s128k":
+        del wsf, wsb
+        torch.cuda.empty_cache()
+        others = workloads_timing(q.device, stream, dfa)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         fl, el, cores, desc = oracle_sample(w, args.cpu_seconds)
-        cpu = {"value": fl / el / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+        rate = fl / el
+        cpu = {"value": rate / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc,
+               # extrapolation, not a measurement: the whole workload's forward + backward
+               # FLOPs at the sampled rate (a row's cost grows with its visible keys)
+               "extrapolated_full_s": flops / rate,
+               "extrapolated_full_note": "extrapolated: full fwd+bwd FLOPs divided by the sampled rate"}
 
     if rank != 0:
         return
@@ -634,9 +819,7 @@ def main():
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype.is_floating_point and w.dtype.itemsize == 2 else "f32",
         "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.H_kv, "S": w.S, "D": w.D,
-                   "n_chunks": w.n_chunks, "sched": args.sched, "causal": True,
-                   "l2": "inputs larger than L2 (each tensor exceeds 129 MB)"},
+        "config": config_of(w, args.sched),
         "pct_of_nominal_bf16_peak": 100.0 * value / world / NOMINAL_BF16_TFLOPS,
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
         # the backward counted at 8D per pair (without recomputing S = QK^T), for other conventions
@@ -644,15 +827,19 @@ def main():
         "roofline": {"bound": "tensor", "kernel": "dfa_attn_bwd (delta + bwd + dQ convert)",
                      "achieved": bwd_tflops, "peak": peak_tc, "unit": "TFLOP/s",
                      "frac": bwd_tflops / peak_tc,
-                     "traffic": NCU_BWD_TRAFFIC.get(w.name) if args.shape is None else None,
+                     "traffic": scaled_traffic(w, "bwd"),
+                     "traffic_note": f"DRAM bytes of one launch captured on {NCU_TRAFFIC_REF['workload']}, "
+                                     "scaled by the ratio of causal pairs (estimate)",
                      "peak_kind": f"{peak_kind} bf16 burst"},
         "roofline_fwd": {"bound": "tensor", "achieved": fwd_tflops, "peak": peak_tc, "unit": "TFLOP/s",
-                         "frac": fwd_tflops / peak_tc},
+                         "frac": fwd_tflops / peak_tc, "traffic": scaled_traffic(w, "fwd")},
         "cpu_baseline": cpu,
         "chunk_step": chunk,
-        "local_window": local,
+        "local_window": local_win,
         "split_kv": split,
         "varlen": varlen,
+        "unbalanced": unbal,
+        "workloads": others,
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clk,

@@ -229,17 +229,19 @@ dfa_status dfa_attn_bwd_varlen(const void* q, const void* k, const void* v, cons
 /* dfa_attn_fwd for callers that cannot allocate device memory.  The paper
  * has no counterpart to this entry point.  Some callers cannot call
  * cudaMalloc where they run attention: a plugin whose host framework owns
- * every byte of device memory, a service that forbids allocation once it is
- * serving, code running while a stream is captured.  This variant takes no
- * workspace: the per-CTA work list lives in a static device array of the
- * library, 2^20 int32 entries (4 MiB) that every GPU which loads the library
- * holds until the process exits.  Same arguments, layouts and results as
- * dfa_attn_fwd without `workspace`/`ws_bytes`.
+ * every byte of device memory, or a service that forbids allocation once it
+ * is serving.  This variant takes no workspace: the per-CTA work list lives
+ * in a static device array of the library, 2^20 int32 entries (4 MiB) that
+ * every GPU which loads the library holds until the process exits.  Same
+ * arguments, layouts and results as dfa_attn_fwd without
+ * `workspace`/`ws_bytes`; for the same schedule the outputs are bit-equal.
  *  - Limit: B*H*ceil(S/256) must not exceed 2^20 - 1025 work items; larger
  *    problems return DFA_ERR_INVALID_ARG without launching anything.
  *  - Set-up: the first bf16 call on a device looks up the array's device
- *    address (with that device current); make that first call before any
- *    stream capture.
+ *    address, with that device current.
+ *  - Not for CUDA graphs: the list is uploaded from a host array shared by
+ *    all calls, so a call on a capturing stream returns DFA_ERR_INVALID_ARG
+ *    and enqueues nothing (dfa_attn_fwd with a workspace can be captured).
  *  - The array is shared by all calls and keeps the last call's contents;
  *    each call rewrites what it uses.  Calls that overlap on the GPU (other
  *    streams or host threads) race on it: serialise them.

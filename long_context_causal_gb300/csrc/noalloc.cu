@@ -3,16 +3,22 @@
 //
 // Some callers cannot call cudaMalloc (or any allocating routine) at the point
 // where they run attention: a framework plugin whose host owns every byte of
-// device memory through its own pool, a service that forbids allocation once
-// it has started serving, or code that runs while a stream is being captured.
-// dfa_attn_fwd needs a caller workspace only for its per-CTA work list; this
-// entry point keeps that list in a fixed file-scope device array instead, so
-// the caller passes only inputs and outputs.
+// device memory through its own pool, or a service that forbids allocation
+// once it has started serving.  dfa_attn_fwd needs a caller workspace only for
+// its per-CTA work list; this entry point keeps that list in a fixed
+// file-scope device array instead, so the caller passes only inputs and
+// outputs.
 //
 // The array is shared by every call in the process and keeps whatever the
 // last call wrote; each call rewrites the part it uses before its kernel
 // reads it.  Calls whose kernels overlap on the GPU (different streams, or
 // several host threads) race on the array.
+//
+// The list is uploaded from a host array shared by all calls, with a pageable
+// copy.  A captured copy would read that array when the graph is replayed,
+// after later calls may have rewritten it for another shape, so a call on a
+// capturing stream is refused (DFA_ERR_INVALID_ARG) before anything is
+// enqueued.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -133,6 +139,13 @@ extern "C" dfa_status dfa_attn_fwd_noalloc(const void* q, const void* k, const v
     p.kv_sb = (int64_t)S * H_kv * D; p.kv_ss = (int64_t)H_kv * D; p.kv_sh = D;
     p.q_offset = 0; p.kv_offset = 0; p.causal = causal != 0; p.scale = scale;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t ce = cudaStreamIsCapturing(s, &cap);
+    if (ce != cudaSuccess) return fail(DFA_ERR_CUDA, "cudaStreamIsCapturing: %s", cudaGetErrorString(ce));
+    if (cap != cudaStreamCaptureStatusNone)
+        return fail(DFA_ERR_INVALID_ARG,
+                    "dfa_attn_fwd_noalloc cannot be captured in a CUDA graph: its work-list upload reads a "
+                    "shared host array when it runs; use dfa_attn_fwd with a workspace under capture");
     dfa_status st;
     if (dt == DFA_F32) {
         st = simt_fwd(p, dt, q, k, v, O, true, lse, s);    // needs no scratch

@@ -130,6 +130,26 @@ def _dense(t: torch.Tensor, name: str):
         raise ValueError(f"{name} must be contiguous (BSHD dense)")
 
 
+def _like(t: torch.Tensor, name: str, shape, dtype, device):
+    """A caller-supplied output must be dense and have exactly the shape, dtype
+    and device the kernels write: a smaller or narrower tensor would be written
+    past its end."""
+    _dense(t, name)
+    if tuple(t.shape) != tuple(shape) or t.dtype != dtype or t.device != device:
+        raise ValueError(f"{name} must be a {dtype} tensor of shape {tuple(shape)} on {device}, "
+                         f"got {t.dtype} {tuple(t.shape)} on {t.device}")
+    return t
+
+
+def _inputs(q, k, v, *rest):
+    """q, k, v (and O, dO where given) share one device; k and v one shape."""
+    if k.shape != v.shape:
+        raise ValueError("k and v must have the same shape")
+    for t in (k, v) + tuple(x for x in rest if x is not None):
+        if t.device != q.device:
+            raise ValueError("all tensors must be on the same device")
+
+
 # ---------------------------------------------------------------- entry points
 def dfa_chunk_attn_fwd(q, k, v, q_offset: int = 0, kv_offset: int = 0, causal: bool = True,
                        scale: float | None = None, O_partial=None, lse=None, stream=None):
@@ -141,10 +161,13 @@ def dfa_chunk_attn_fwd(q, k, v, q_offset: int = 0, kv_offset: int = 0, causal: b
     if q.stride(3) != 1 or k.stride(3) != 1:
         raise ValueError("the head dimension must be contiguous")
     scale = D ** -0.5 if scale is None else float(scale)
+    _inputs(q, k, v)
     if O_partial is None:
         O_partial = torch.empty((B, Lq, H, D), dtype=torch.float32, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, Lq), dtype=torch.float32, device=q.device)
+    _like(O_partial, "O_partial", (B, Lq, H, D), torch.float32, q.device)
+    _like(lse, "lse", (B, H, Lq), torch.float32, q.device)
     qs = (ctypes.c_int64 * 3)(q.stride(0), q.stride(1), q.stride(2))
     ks = (ctypes.c_int64 * 3)(k.stride(0), k.stride(1), k.stride(2))
     _check(_lib.dfa_chunk_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _dtype(q), B, H, Hkv, Lq, Lkv, D,
@@ -172,10 +195,13 @@ def dfa_chunk_attn_bwd(q, k, v, O, lse, dO, q_offset: int = 0, kv_offset: int = 
     dQ_acc = torch.zeros((B, Lq, H, D), **f32) if dQ_acc is None else dQ_acc
     dK_acc = torch.zeros((B, Lkv, Hkv, D), **f32) if dK_acc is None else dK_acc
     dV_acc = torch.zeros((B, Lkv, Hkv, D), **f32) if dV_acc is None else dV_acc
-    for t, n in ((dQ_acc, "dQ_acc"), (dK_acc, "dK_acc"), (dV_acc, "dV_acc")):
-        _dense(t, n)
-        if t.dtype != torch.float32:
-            raise ValueError(f"{n} must be fp32")
+    _inputs(q, k, v, O, dO, lse)
+    _like(O, "O", q.shape, q.dtype, q.device)
+    _like(dO, "dO", q.shape, q.dtype, q.device)
+    _like(lse, "lse", (B, H, Lq), torch.float32, q.device)
+    _like(dQ_acc, "dQ_acc", (B, Lq, H, D), torch.float32, q.device)
+    _like(dK_acc, "dK_acc", (B, Lkv, Hkv, D), torch.float32, q.device)
+    _like(dV_acc, "dV_acc", (B, Lkv, Hkv, D), torch.float32, q.device)
     if workspace_buf is None:
         workspace_buf = torch.empty(max(dfa_chunk_bwd_workspace_size(B, H, Hkv, Lq, Lkv, D), 16),
                                     dtype=torch.uint8, device=q.device)
@@ -191,8 +217,14 @@ def dfa_merge_partials(O_a, lse_a, O_b, lse_b, O_out=None, lse_out=None, stream=
     B, L, H, D = O_a.shape
     for t, n in ((O_a, "O_a"), (O_b, "O_b"), (lse_a, "lse_a"), (lse_b, "lse_b")):
         _dense(t, n)
+    for t, n in ((O_a, "O_a"), (O_b, "O_b")):
+        _like(t, n, (B, L, H, D), torch.float32, O_a.device)
+    for t, n in ((lse_a, "lse_a"), (lse_b, "lse_b")):
+        _like(t, n, (B, H, L), torch.float32, O_a.device)
     O_out = torch.empty_like(O_a) if O_out is None else O_out
     lse_out = torch.empty_like(lse_a) if lse_out is None else lse_out
+    _like(O_out, "O_out", (B, L, H, D), torch.float32, O_a.device)
+    _like(lse_out, "lse_out", (B, H, L), torch.float32, O_a.device)
     _check(_lib.dfa_merge_partials(B, H, L, D, _ptr(O_a), _ptr(lse_a), _ptr(O_b), _ptr(lse_b),
                                    _ptr(O_out), _ptr(lse_out), _stream(stream)))
     return O_out, lse_out
@@ -215,8 +247,10 @@ def dfa_attn_fwd(q, k, v, n_chunks: int = 1, causal: bool = True, scale: float |
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _dense(t, n)
     scale = D ** -0.5 if scale is None else float(scale)
-    O = torch.empty_like(q) if O is None else O
-    lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device) if lse is None else lse
+    _inputs(q, k, v)
+    O = torch.empty_like(q) if O is None else _like(O, "O", q.shape, q.dtype, q.device)
+    lse = (torch.empty((B, H, S), dtype=torch.float32, device=q.device) if lse is None
+           else _like(lse, "lse", (B, H, S), torch.float32, q.device))
     ws = workspace(B, H, Hkv, S, D, n_chunks, False, q.device) if workspace_buf is None else workspace_buf
     _check(_lib.dfa_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _dtype(q), B, H, Hkv, S, D, int(n_chunks),
                              int(bool(causal)), scale, _SCHED[sched], _ptr(O), _ptr(lse), _ptr(ws),
@@ -264,8 +298,10 @@ def dfa_attn_fwd_varlen(q, k, v, cu_seqlens, causal: bool = True, scale: float |
     cu = _cu_host(cu_seqlens)
     _check_packed(cu, T)
     scale = D ** -0.5 if scale is None else float(scale)
-    O = torch.empty_like(q) if O is None else O
-    lse = torch.empty((H, T), dtype=torch.float32, device=q.device) if lse is None else lse
+    _inputs(q, k, v)
+    O = torch.empty_like(q) if O is None else _like(O, "O", q.shape, q.dtype, q.device)
+    lse = (torch.empty((H, T), dtype=torch.float32, device=q.device) if lse is None
+           else _like(lse, "lse", (H, T), torch.float32, q.device))
     ws = varlen_workspace(cu, H, Hkv, D, False, q.device) if workspace_buf is None else workspace_buf
     _check(_lib.dfa_attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _dtype(q), _p32(cu), cu.size - 1, H, Hkv, D,
                                     int(bool(causal)), scale, _ptr(O), _ptr(lse), _ptr(ws), ws.numel(),
@@ -283,9 +319,13 @@ def dfa_attn_bwd_varlen(q, k, v, O, lse, dO, cu_seqlens, causal: bool = True, sc
     cu = _cu_host(cu_seqlens)
     _check_packed(cu, T)
     scale = D ** -0.5 if scale is None else float(scale)
-    dQ = torch.empty_like(q) if dQ is None else dQ
-    dK = torch.empty_like(k) if dK is None else dK
-    dV = torch.empty_like(v) if dV is None else dV
+    _inputs(q, k, v, O, dO, lse)
+    _like(O, "O", q.shape, q.dtype, q.device)
+    _like(dO, "dO", q.shape, q.dtype, q.device)
+    _like(lse, "lse", (H, T), torch.float32, q.device)
+    dQ = torch.empty_like(q) if dQ is None else _like(dQ, "dQ", q.shape, q.dtype, q.device)
+    dK = torch.empty_like(k) if dK is None else _like(dK, "dK", k.shape, q.dtype, q.device)
+    dV = torch.empty_like(v) if dV is None else _like(dV, "dV", v.shape, q.dtype, q.device)
     ws = varlen_workspace(cu, H, Hkv, D, True, q.device) if workspace_buf is None else workspace_buf
     _check(_lib.dfa_attn_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(O), _ptr(lse), _ptr(dO), _dtype(q),
                                     _p32(cu), cu.size - 1, H, Hkv, D, int(bool(causal)), scale,
@@ -298,8 +338,11 @@ def dfa_attn_fwd_noalloc(q, k, v, O, lse, n_chunks: int = 1, causal: bool = True
     """dfa_attn_fwd without a workspace: writes the caller's O and lse, allocates nothing."""
     B, S, H, D = q.shape
     Hkv = k.shape[2]
-    for t, n in ((q, "q"), (k, "k"), (v, "v"), (O, "O"), (lse, "lse")):
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _dense(t, n)
+    _inputs(q, k, v)
+    _like(O, "O", q.shape, q.dtype, q.device)
+    _like(lse, "lse", (B, H, S), torch.float32, q.device)
     scale = D ** -0.5 if scale is None else float(scale)
     _check(_lib.dfa_attn_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _dtype(q), B, H, Hkv, S, D, int(n_chunks),
                                      int(bool(causal)), scale, _SCHED[sched], _ptr(O), _ptr(lse),
@@ -316,9 +359,13 @@ def dfa_attn_bwd(q, k, v, O, lse, dO, n_chunks: int = 1, causal: bool = True,
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (O, "O"), (lse, "lse"), (dO, "dO")):
         _dense(t, n)
     scale = D ** -0.5 if scale is None else float(scale)
-    dQ = torch.empty_like(q) if dQ is None else dQ
-    dK = torch.empty_like(k) if dK is None else dK
-    dV = torch.empty_like(v) if dV is None else dV
+    _inputs(q, k, v, O, dO, lse)
+    _like(O, "O", q.shape, q.dtype, q.device)
+    _like(dO, "dO", q.shape, q.dtype, q.device)
+    _like(lse, "lse", (B, H, S), torch.float32, q.device)
+    dQ = torch.empty_like(q) if dQ is None else _like(dQ, "dQ", q.shape, q.dtype, q.device)
+    dK = torch.empty_like(k) if dK is None else _like(dK, "dK", k.shape, q.dtype, q.device)
+    dV = torch.empty_like(v) if dV is None else _like(dV, "dV", v.shape, q.dtype, q.device)
     ws = workspace(B, H, Hkv, S, D, n_chunks, True, q.device) if workspace_buf is None else workspace_buf
     _check(_lib.dfa_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(O), _ptr(lse), _ptr(dO), _dtype(q),
                              B, H, Hkv, S, D, int(n_chunks), int(bool(causal)), scale, _SCHED[sched],
@@ -336,8 +383,10 @@ def dfa_attn_fwd_local(q, k, v, n_chunks: int, window: int, scale: float | None 
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _dense(t, n)
     scale = D ** -0.5 if scale is None else float(scale)
-    O = torch.empty_like(q) if O is None else O
-    lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device) if lse is None else lse
+    _inputs(q, k, v)
+    O = torch.empty_like(q) if O is None else _like(O, "O", q.shape, q.dtype, q.device)
+    lse = (torch.empty((B, H, S), dtype=torch.float32, device=q.device) if lse is None
+           else _like(lse, "lse", (B, H, S), torch.float32, q.device))
     ws = workspace(B, H, Hkv, S, D, n_chunks, False, q.device) if workspace_buf is None else workspace_buf
     _check(_lib.dfa_attn_fwd_local(_ptr(q), _ptr(k), _ptr(v), _dtype(q), B, H, Hkv, S, D, int(n_chunks),
                                    int(window), scale, _SCHED[sched], _ptr(O), _ptr(lse), _ptr(ws), ws.numel(),
@@ -353,9 +402,13 @@ def dfa_attn_bwd_local(q, k, v, O, lse, dO, n_chunks: int, window: int, scale: f
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (O, "O"), (lse, "lse"), (dO, "dO")):
         _dense(t, n)
     scale = D ** -0.5 if scale is None else float(scale)
-    dQ = torch.empty_like(q) if dQ is None else dQ
-    dK = torch.empty_like(k) if dK is None else dK
-    dV = torch.empty_like(v) if dV is None else dV
+    _inputs(q, k, v, O, dO, lse)
+    _like(O, "O", q.shape, q.dtype, q.device)
+    _like(dO, "dO", q.shape, q.dtype, q.device)
+    _like(lse, "lse", (B, H, S), torch.float32, q.device)
+    dQ = torch.empty_like(q) if dQ is None else _like(dQ, "dQ", q.shape, q.dtype, q.device)
+    dK = torch.empty_like(k) if dK is None else _like(dK, "dK", k.shape, q.dtype, q.device)
+    dV = torch.empty_like(v) if dV is None else _like(dV, "dV", v.shape, q.dtype, q.device)
     ws = workspace(B, H, Hkv, S, D, n_chunks, True, q.device) if workspace_buf is None else workspace_buf
     _check(_lib.dfa_attn_bwd_local(_ptr(q), _ptr(k), _ptr(v), _ptr(O), _ptr(lse), _ptr(dO), _dtype(q),
                                    B, H, Hkv, S, D, int(n_chunks), int(window), scale, _SCHED[sched],

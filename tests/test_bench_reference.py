@@ -32,6 +32,11 @@ def test_reference_line_keeps_the_contract():
     assert d["value"] > 0 and d["higher_is_better"] is True and d["vs_baseline"] is None
     assert d["steps"] == 1 and d["warmup"] == 0 and d["n_gpus"] == 1 and d["ms_per_step"] > 0
     assert d["config"]["workload"] == "llama7b_s32k" and d["config"]["S"] == 32768
+    # the same config object as the GPU arm prints for this workload, so the two lines compare
+    sys.path.insert(0, ROOT)
+    import bench
+    from long_context_causal_gb300.inputs import WORKLOADS
+    assert d["config"] == bench.config_of(WORKLOADS["llama7b_s32k"], "balanced")
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
     e = d["e2e"]
