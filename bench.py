@@ -256,6 +256,8 @@ def chunk_step_timing(w, q, k, v, O, lse, do, stream, dfa, reps=5):
     if w.n_chunks < 2:
         return None
     C = -(-w.S // w.n_chunks)     # the library's chunk length: ceil(S / n_chunks), the last chunk shorter
+    last = (w.n_chunks - 1) * C   # first token of the last chunk
+    Cq = w.S - last
     out = {"C": C}
     f32 = dict(dtype=torch.float32, device=q.device)
     ws = torch.empty(max(dfa.dfa_chunk_bwd_workspace_size(w.B, w.H, w.H_kv, Cq, C, w.D), 16),
@@ -264,8 +266,6 @@ def chunk_step_timing(w, q, k, v, O, lse, do, stream, dfa, reps=5):
     lp = torch.empty((w.B, w.H, Cq), **f32)
     acc = (torch.zeros((w.B, Cq, w.H, w.D), **f32), torch.zeros((w.B, C, w.H_kv, w.D), **f32),
            torch.zeros((w.B, C, w.H_kv, w.D), **f32))
-    last = (w.n_chunks - 1) * C   # first token of the last chunk
-    Cq = w.S - last
     for name, (qa, ka, Lk) in (("off_diagonal", (last, 0, C)), ("diagonal", (last, last, Cq))):
         qs, ks = slice(qa, qa + Cq), slice(ka, ka + Lk)
         qc, kc, vc, dc = (t.contiguous() for t in (q[:, qs], k[:, ks], v[:, ks], do[:, qs]))

@@ -108,10 +108,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 // Out-of-line bounded wait (keeps cold wait loops out of the hot code) and
 // its traced form, which also adds the SM cycles it spent (including the
 // blocking first try_wait) to *acc_cycles: the per-role wait profile of the
-// trace facility.
+// trace facility.  R selects a separate copy of the function: a kernel whose
+// warpgroups run under different setmaxnreg budgets needs one copy per
+// budget (one out-of-line function cannot be compiled for two budgets).
+template <int R = 0>
 static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err) {
     return mbar_wait(bar, parity, abort_flag, err);
 }
+template <int R = 0>
 static __device__ __noinline__ bool mbar_wait_traced(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err,
                                               uint64_t* acc_cycles) {
     const uint64_t t0 = clock64();
@@ -134,16 +138,18 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
 // Wait for the MMA issuer: a plain test first (the common case is a phase that
 // has already completed, and a potentially-suspending try_wait there leaves the
 // tensor pipe idle for hundreds of cycles), then the bounded blocking wait.
+template <int R = 0>
 __device__ __forceinline__ bool mbar_wait_issuer(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                                  int* err) {
     if (mbar_test_wait(bar, parity)) return true;
-    return mbar_wait_slow(bar, parity, abort_flag, err);
+    return mbar_wait_slow<R>(bar, parity, abort_flag, err);
 }
+template <int R = 0>
 __device__ __forceinline__ bool mbar_wait_acc(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                               int* err, uint64_t* acc_cycles) {
-    if (acc_cycles) return mbar_wait_traced(bar, parity, abort_flag, err, acc_cycles);
+    if (acc_cycles) return mbar_wait_traced<R>(bar, parity, abort_flag, err, acc_cycles);
     if (mbar_try_wait(bar, parity)) return true;
-    return mbar_wait_slow(bar, parity, abort_flag, err);
+    return mbar_wait_slow<R>(bar, parity, abort_flag, err);
 }
 
 // Bulk (TMA) fp32 reduction of a contiguous shared-memory block into global
