@@ -20,15 +20,20 @@
 //   P/dS warps per tile:   phase1(n), phase2(n), phase1(n+1), ...
 // All MMAs are N = 128 or 128-row wide (few, large instructions: one thread
 // issues them all).  Two warpgroups split the 128 query columns (two warps
-// per SM sub-partition hide each other's latency); a third drains dQ.
+// per SM sub-partition hide each other's latency); two more drain dQ.
 //
 // TMEM columns: dV [0,128) dK [128,256) S^T [256,384) (P^T of query half h at
 // [256+64h, 256+64h+32)), dP^T / dQ^T [384,512).
-// Roles (512 threads, one CTA per SM, persistent over the work list):
+// Roles (640 threads, one CTA per SM, persistent over the work list):
 // warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM owner, warps 4-11
-// P/dS (two warpgroups by query half) and the dK/dV epilogue, warps 12-15
-// dQ drain (dQ^T out of TMEM, 16-byte fp32 reductions; a warp instruction
-// covers four full 128-byte dQ rows).
+// P/dS (two warpgroups by query half) and the dK/dV epilogue, warps 12-19
+// dQ drain (two warpgroups by query half: dQ^T out of TMEM, 16-byte fp32
+// reductions; a warp instruction covers four full 128-byte dQ rows).
+// dQ^T shares its TMEM columns with the next tile's dP^T, so the drain reads
+// all of its 64 columns into registers and releases the columns before any
+// reduction: the next dP^T then waits for two TMEM loads, not for 64 KB of
+// reductions.  The registers for that come from a setmaxnreg split (the
+// control warpgroup needs few).
 // Trace wait slots (cycles): 0 P/dS dP^T, 1 MMA inputs, 2 MMA dq_free,
 // 3 MMA P^T done, 4 MMA dS^T done, 5 P/dS Q + S^T, 6 P/dS accumulators, 7 drain.
 #include <cuda.h>
@@ -45,7 +50,7 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 640;
 constexpr int BT = 128;          // key rows per work item; query rows per tile
 constexpr int D = 128;
 constexpr int kTile = BT * D * 2;                  // 32 KB bf16 tile
@@ -57,6 +62,15 @@ constexpr int kSmem = kOffBar + 256;
 static_assert(kSmem <= 232448, "shared memory");
 
 constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384;
+
+// Register split (setmaxnreg).  The kernel launches with kLaunchRegs per
+// thread (640 x 96 = 61440); the control warpgroup (TMA, MMA, TMEM owner, one
+// idle warp) and the two dQ drain warpgroups give registers up, the two P/dS
+// warpgroups take them: 128 x 64 + 256 x 128 + 256 x 80 = 61440.  A drain
+// thread holds its 64 dQ^T values at once.
+constexpr uint32_t kLaunchRegs = 96, kCtrlRegs = 64, kPdsRegs = 128, kDrainRegs = 80;
+static_assert(kThreads * kLaunchRegs <= 65536, "launch register file");
+static_assert(128 * kCtrlRegs + 256 * kPdsRegs + 256 * kDrainRegs <= kThreads * kLaunchRegs, "register split");
 
 struct Args {
     int B, H, Hkv, Lq, Lkv, S_pad, causal;
@@ -207,7 +221,7 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         mbar_init(p_done, 2 * BT);
         mbar_init(ds_done, 2 * BT);
         mbar_init(dq_full, 1);
-        mbar_init(dq_free, BT);
+        mbar_init(dq_free, 2 * BT);
         mbar_init(kd_full, 1);
         mbar_init(kd_empty, 2 * BT);
         mbar_init(done, 1);
@@ -228,6 +242,11 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const uint32_t tmem = *tmem_slot;
     const uint64_t t_start = globaltimer();
 
+    // Every warp of a warpgroup executes its warpgroup's setmaxnreg, and each
+    // role's code sits inside the branch that set its budget (code reached
+    // under two budgets cannot be shared, hence one barrier copy per branch).
+    if (warp < 4) {
+    setmaxnreg_dec<kCtrlRegs>();
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         uint32_t n = 0, kvi = 0, kv_issued = 0, q_issued = 0, do_issued = 0;
@@ -388,7 +407,14 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             trace_count(a.trace, a.trace_cap, 4, n);
             for (int z = 0; z < 4; ++z) trace_wait(a.trace, a.trace_cap, 1 + z, wt[z]);
         }
-    } else if (warp >= 4 && warp < 12) {
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 2) tmem_dealloc(tmem, 512);
+    if (threadIdx.x == 0) trace_cta(a.trace, a.trace_cap, t_start, it_end - it_begin);
+    } else if (warp < 12) {
+        setmaxnreg_inc<kPdsRegs>();
         // ------------------------------------------------------------ P^T / dS^T, dK/dV epilogue
         const int half = (warp - 4) / 4;                   // query columns [64 half, 64 half + 64)
         const int r = (warp % 4) * 32 + lane;              // key row == TMEM lane
@@ -401,7 +427,7 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         uint64_t wt[3] = {0, 0, 0};   // Q/S^T, dK/dV accumulators, dP^T
         auto wait = [&](uint64_t* bar, uint32_t parity, int slot) {
             ok = ok && __all_sync(0xffffffffu,
-                                  mbar_wait_acc(bar, parity, abort_flag, a.err, a.trace ? &wt[slot] : nullptr));
+                                  mbar_wait_acc<1>(bar, parity, abort_flag, a.err, a.trace ? &wt[slot] : nullptr));
             return ok;
         };
         for (int it = it_begin; it < it_end && ok; ++it) {
@@ -552,10 +578,15 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             trace_wait(a.trace, a.trace_cap, 6, wt[1]);
             trace_wait(a.trace, a.trace_cap, 0, wt[2]);
         }
-    } else if (warp >= 12) {
+        tc_fence_before();
+        __syncthreads();
+    } else {
+        setmaxnreg_dec<kDrainRegs>();
         // ------------------------------------------------------------ dQ drain
         // TMEM lane = head-dim element of dQ^T; column c = query row i*128 + c.
-        const uint32_t tdQ = tmem + ((uint32_t)((warp % 4) * 32) << 16) + kColDP;
+        // Two warpgroups: warpgroup dg drains query columns [64 dg, 64 dg + 64).
+        const int dg = (warp - 12) / 4;
+        const uint32_t tdQ = tmem + ((uint32_t)((warp % 4) * 32) << 16) + kColDP + dg * 64;
         uint32_t n = 0;
         bool ok = true;
         uint64_t wt = 0;
@@ -566,7 +597,7 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             for (int k = 0; k < x.ntiles; ++k, ++n) {
                 int h, i;
                 x.tile(k, G, h, i);
-                ok = __all_sync(0xffffffffu, mbar_wait_acc(dq_full, n & 1, abort_flag, a.err, a.trace ? &wt : nullptr));
+                ok = __all_sync(0xffffffffu, mbar_wait_acc<2>(dq_full, n & 1, abort_flag, a.err, a.trace ? &wt : nullptr));
                 if (!ok) break;
                 tc_fence_after();
                 // dQ accumulator is head-major [B, H, S, D]: the tile is one contiguous
@@ -578,26 +609,21 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 float* base = a.dq_acc + (((int64_t)SEQ_TB(x) * a.H + h) * (VARLEN ? a.acc_rows : a.Lq) + s_pbase +
                                           (int64_t)i * BT + m) * D +
                               (warp % 4) * 32 + (lane >> 2) * 4;
-                const int nq = min(BT, s_len - i * BT);
-                // Two halves of 64 query columns (64 registers each); TMEM is
-                // released once the second half has been read.
-#pragma unroll 1
-                for (int hf = 0; hf < 2; ++hf) {
-                    uint32_t v[64];
-                    tmem_ld32x2(tdQ + hf * 64, tdQ + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[0]),
-                                *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-                    if (hf == 1) {   // relaxed: the arrival must not wait for the first half's adds
-                        tc_fence_before();
-                        mbar_arrive_relaxed(dq_free);
-                    }
+                const int nq = min(BT, s_len - i * BT) - dg * 64;
+                // This warpgroup's 64 query columns are read at once, then TMEM is
+                // released (relaxed: the arrival must not wait for any reduction).
+                uint32_t v[64];
+                tmem_ld32x2(tdQ, tdQ + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[0]),
+                            *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+                tc_fence_before();
+                mbar_arrive_relaxed(dq_free);
 #pragma unroll
-                    for (int g = 0; g < 16; ++g) {
-                        float xq[4] = {__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
-                                       __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3])};
-                        quad_transpose(xq, lane);
-                        if (hf * 64 + 4 * g + m < nq)
-                            red_add_v4(base + (hf * 64 + 4 * g) * D, xq[0], xq[1], xq[2], xq[3]);
-                    }
+                for (int g = 0; g < 16; ++g) {
+                    float xq[4] = {__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
+                                   __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3])};
+                    quad_transpose(xq, lane);
+                    if (4 * g + m < nq)
+                        red_add_v4(base + (dg * 64 + 4 * g) * D, xq[0], xq[1], xq[2], xq[3]);
                 }
             }
         }
@@ -605,12 +631,9 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             trace_count(a.trace, a.trace_cap, 7, n);
             trace_wait(a.trace, a.trace_cap, 7, wt);
         }
+        tc_fence_before();
+        __syncthreads();
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 2) tmem_dealloc(tmem, 512);
-    if (threadIdx.x == 0) trace_cta(a.trace, a.trace_cap, t_start, it_end - it_begin);
 }
 
 #undef SEQ_LQ
@@ -656,6 +679,12 @@ dfa_status tc_bwd_pipelined(const AttnProblem& p, const void* q, const void* k, 
     auto kern = p.seq ? bwd_pipe_kernel<true, false> : split ? bwd_pipe_kernel<false, true> : bwd_pipe_kernel<false, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
         return fail(DFA_ERR_CUDA, "bwd_pipe: shared memory attribute");
+    // The setmaxnreg split assumes the launch register count; a different
+    // count could leave a warpgroup's register increase waiting forever.
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || fa.numRegs != (int)kLaunchRegs)
+        return fail(DFA_ERR_CUDA, "bwd_pipe: built with %d registers per thread, the register split needs %u",
+                    fa.numRegs, kLaunchRegs);
     kern<<<wl->n_workers, kThreads, kSmem, s>>>(mq, mk, mv, mdo, a);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? DFA_OK : fail(DFA_ERR_CUDA, "bwd_pipe launch: %s", cudaGetErrorString(e));

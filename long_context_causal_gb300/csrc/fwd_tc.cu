@@ -24,8 +24,6 @@
 //
 // TMEM columns: S_0 [0,128) S_1 [128,256) O_0 [256,256+D) O_1 [384,384+D);
 // P_w (bf16 pairs) overwrites the first 64 columns of S_w.
-// Trace wait slots (cycles, with the CTA trace on): 1 MMA inputs, 2 MMA P
-// ready, 5 softmax S ready, 7 softmax work (S ready to P released).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -332,10 +330,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 for (int kk = 1; kk < BN / 16; ++kk) mma_ts(d, a + kk * 8, b0 + kk * (2048 >> 4), idO, 1u);
             }
         };
-        uint64_t wt[2] = {0, 0};   // trace only: cycles waiting for inputs, for P
-        auto wait = [&](uint64_t* bar, uint32_t parity, int slot = 0) {
-            ok = ok && (a.trace ? mbar_wait_acc(bar, parity, abort_flag, a.err, &wt[slot])
-                                : mbar_wait_issuer(bar, parity, abort_flag, a.err));
+        auto wait = [&](uint64_t* bar, uint32_t parity) {
+            ok = ok && mbar_wait_issuer(bar, parity, abort_flag, a.err);
             if (ok) tc_fence_after();
             return ok;
         };
@@ -356,7 +352,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 const bool more = j + 1 < x.n_kv;
                 const uint32_t slotV = cons % C::kSlots;
                 if (!wait(&kv_full[slotV], (cons / C::kSlots) & 1)) break;
-                if (!wait(&p_full[0], t & 1, 1)) break;
+                if (!wait(&p_full[0], t & 1)) break;
                 issue_PV(0, slotV, j > x.j0);
                 if (!more) commit(&o_full[0]);
                 uint32_t slotK1 = (cons + 1) % C::kSlots;
@@ -365,7 +361,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     issue_S(0, slotK1);
                     commit(&s_full[0]);
                 }
-                if (!wait(&p_full[1], t & 1, 1)) break;
+                if (!wait(&p_full[1], t & 1)) break;
                 issue_PV(1, slotV, j > x.j0);
                 commit(&kv_empty[slotV]);
                 if (!more) commit(&o_full[1]);
@@ -385,8 +381,6 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         int dummy = 0;
         mbar_wait(done, 0, &dummy, a.err);
         trace_count(a.trace, a.trace_cap, 4, t);
-        trace_wait(a.trace, a.trace_cap, 1, wt[0]);
-        trace_wait(a.trace, a.trace_cap, 2, wt[1]);
     } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax warpgroups
         const int w = (warp - 4) / 4;                 // which query tile
@@ -397,7 +391,6 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const float c2 = a.scale_log2;
         uint32_t t = 0, qi = 0;
         bool ok = true;
-        uint64_t wt_s = 0, wt_c = 0;   // trace only: cycles waiting for S, cycles of softmax work
         for (int it = it_begin; it < it_end && ok; ++it) {
             const Item x = decode(a, a.wl_items ? a.wl_items[it] : it, WIN);
             const int row = x.q0 + w * BM + r;                 // row within the query chunk
@@ -408,10 +401,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             const int64_t lo_row = WIN ? window_lo(a, qpos) - a.kv_offset : INT64_MIN;
             const int64_t lo_tile = WIN ? window_lo(a, a.q_offset + x.q0 + w * BM + BM - 1) - a.kv_offset : INT64_MIN;
             for (int j = x.j0; j < x.n_kv; ++j, ++t) {
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait_acc(&s_full[w], t & 1, abort_flag, a.err, a.trace ? &wt_s : nullptr));
+                ok = __all_sync(0xffffffffu, mbar_wait_acc(&s_full[w], t & 1, abort_flag, a.err, nullptr));
                 if (!ok) break;
-                const uint64_t c_soft = a.trace ? clock64() : 0;
                 tc_fence_after();
                 // Pass 1: row max over the tile (S read from TMEM 32 columns at a time).
                 const int kv0 = j * BN;
@@ -461,7 +452,6 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(&p_full[w]);
-                if (a.trace) wt_c += clock64() - c_soft;
             }
             if (!ok) break;
             // ---- epilogue: O = O_acc / l, lse = ln(sum exp(s))
@@ -509,11 +499,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             if (valid_row)
                 a.lse[((int64_t)x.tb * a.H + x.h) * a.Lq + x.base + row + x.s * a.lse_piece_stride] = l > 0.f ? (m_run + __log2f(l)) * kLn2 : -INFINITY;
         }
-        if (threadIdx.x == 128) {
-            trace_count(a.trace, a.trace_cap, 5, t);
-            trace_wait(a.trace, a.trace_cap, 5, wt_s);
-            trace_wait(a.trace, a.trace_cap, 7, wt_c);
-        }
+        if (threadIdx.x == 128) trace_count(a.trace, a.trace_cap, 5, t);
     }
     tc_fence_before();
     __syncthreads();
