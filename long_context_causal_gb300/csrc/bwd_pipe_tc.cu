@@ -328,7 +328,7 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         uint64_t wt[4] = {0, 0, 0, 0};   // inputs (Q, dO, K/V, dK/dV free), dq_free, P^T, dS^T
         auto wait = [&](uint64_t* bar, uint32_t parity, int slot) {
             ok = ok && (a.trace ? mbar_wait_acc(bar, parity, abort_flag, a.err, &wt[slot])
-                                : mbar_wait_issuer(bar, parity, abort_flag, a.err));
+                                : mbar_wait_spin(bar, parity, abort_flag, a.err));
             if (ok) tc_fence_after();
             return ok;
         };

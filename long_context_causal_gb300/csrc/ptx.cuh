@@ -135,6 +135,26 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// Waits by polling test_wait, never suspending the thread, bounded like
+// mbar_wait.  For an MMA-issuing thread whose waits are usually short: a
+// suspended try_wait resumes a few hundred cycles after the phase completes,
+// which leaves the tensor pipe without queued work (measured on the backward:
+// about 5% of its time).
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if ((i & 63u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                if (err) atomicExch(err, kErrTimeout);
+                return false;
+            }
+        }
+    }
+}
 // Wait for the MMA issuer: a plain test first (the common case is a phase that
 // has already completed, and a potentially-suspending try_wait there leaves the
 // tensor pipe idle for hundreds of cycles), then the bounded blocking wait.
