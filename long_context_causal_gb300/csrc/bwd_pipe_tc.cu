@@ -316,13 +316,15 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         constexpr uint32_t idS = idesc_bf16_f32(BT, BT, false, false);   // S^T, dP^T
         constexpr uint32_t idKM = idesc_bf16_f32(BT, D, false, true);    // dV, dK: B N-major
         constexpr uint32_t idQ = idesc_bf16_f32(D, BT, true, true);      // dQ^T: M = head dim
-        const uint64_t dKk = sdesc_sw128(smem_u32(sK), 16, 1024), dKn = sdesc_sw128(smem_u32(sK), 16384, 1024);
-        const uint64_t dVk = sdesc_sw128(smem_u32(sV), 16, 1024);
-        const uint64_t dQk = sdesc_sw128(smem_u32(sQ), 16, 1024), dQn = sdesc_sw128(smem_u32(sQ), 16384, 1024);
-        const uint64_t dOk = sdesc_sw128(smem_u32(sdO), 16, 1024), dOn = sdesc_sw128(smem_u32(sdO), 16384, 1024);
-        const uint64_t dSk = sdesc_sw128(smem_u32(sdS), 16, 1024), dSn = sdesc_sw128(smem_u32(sdS), 16384, 1024);
-        constexpr uint64_t kSlot = kTile >> 4, kRows16 = 2048 >> 4;
-        auto kmaj = [](int kk) -> uint64_t { return (uint64_t)(((kk / 4) * 16384 + (kk % 4) * 32) >> 4); };
+        // Descriptors as SDesc words: moved by 32-bit adds on the low word.
+        auto desc = [](const void* p, uint32_t lbo) { return sdesc_words(sdesc_sw128(smem_u32(p), lbo, 1024)); };
+        const SDesc dKk = desc(sK, 16), dKn = desc(sK, 16384);
+        const SDesc dVk = desc(sV, 16);
+        const SDesc dQk = desc(sQ, 16), dQn = desc(sQ, 16384);
+        const SDesc dOk = desc(sdO, 16), dOn = desc(sdO, 16384);
+        const SDesc dSk = desc(sdS, 16), dSn = desc(sdS, 16384);
+        constexpr uint32_t kSlot = kTile >> 4, kRows16 = 2048 >> 4;
+        auto kmaj = [](int kk) -> uint32_t { return (uint32_t)(((kk / 4) * 16384 + (kk % 4) * 32) >> 4); };
         uint32_t n = 0, kvi = 0;
         bool ok = true;
         uint64_t wt[4] = {0, 0, 0, 0};   // inputs (Q, dO, K/V, dK/dV free), dq_free, P^T, dS^T
@@ -337,7 +339,7 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const uint32_t s = m & 1;
             if (!wait(&q_full[s], (m >> 1) & 1, 0)) return false;
             {
-                const uint64_t b0 = dQk + s * kSlot;
+                const SDesc b0 = dQk + s * kSlot;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + kColS, dKk + kmaj(kk), b0 + kmaj(kk), idS, kk > 0);
             }
@@ -349,7 +351,7 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             if (!wait(&do_full[s], (m >> 1) & 1, 0)) return false;
             if (m > 0 && !wait(dq_free, (m - 1) & 1, 1)) return false;
             {
-                const uint64_t b0 = dOk + s * kSlot;
+                const SDesc b0 = dOk + s * kSlot;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + kColDP, dVk + kmaj(kk), b0 + kmaj(kk), idS, kk > 0);
             }
@@ -368,7 +370,7 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 if (!wait(p_done, n & 1, 2)) break;
                 const uint32_t acc0 = k > 0 ? 1u : 0u;
                 {   // dV += P^T dO: P^T of query half h at S + 64h
-                    const uint64_t b0 = dOn + s * kSlot;
+                    const SDesc b0 = dOn + s * kSlot;
 #pragma unroll
                     for (int kk = 0; kk < BT / 16; ++kk)
                         mma_ts(tmem + kColDV, tmem + kColS + kk * 8 + (kk >= 4 ? 32 : 0), b0 + kk * kRows16, idKM,
@@ -384,7 +386,7 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 }
                 commit(dq_full);
                 {   // dK += dS^T Q
-                    const uint64_t bq = dQn + s * kSlot;
+                    const SDesc bq = dQn + s * kSlot;
 #pragma unroll
                     for (int kk = 0; kk < BT / 16; ++kk)
                         mma_ss(tmem + kColDK, dSk + kmaj(kk), bq + kk * kRows16, idKM, kk > 0 ? 1u : acc0);

@@ -293,6 +293,22 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
            | ((uint32_t)(M >> 4) << 24);  // M / 16
 }
 
+// A shared-memory matrix descriptor held as its two 32-bit words.  The
+// start-address field is the low word's bits 0-13 (address >> 4, below 2^14
+// for every shared address under 256 KB), so moving a descriptor within
+// shared memory is one 32-bit add on the low word that never carries into the
+// high word.  The issuing thread competes for issue slots with the busy warps
+// of its SM sub-partition, so each instruction it saves per MMA shows: in a
+// stand-alone issue loop beside softmax-like warps, 64-bit descriptor adds ran
+// at 71.6 cycles per 128x128x16 MMA and these 32-bit adds at 68.1 (64 alone);
+// the backward kernel's 128K pass went from 327 to 316 ms with them.  (The
+// forward's issue loop measured slower with them and keeps 64-bit adds.)
+struct SDesc {
+    uint32_t lo, hi;
+};
+__device__ __forceinline__ SDesc sdesc_words(uint64_t d) { return SDesc{(uint32_t)d, (uint32_t)(d >> 32)}; }
+__device__ __forceinline__ SDesc operator+(SDesc d, uint32_t off) { return SDesc{d.lo + off, d.hi}; }
+
 // D[tmem] (+)= A[smem desc] * B[smem desc]; single thread.
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                        uint32_t accumulate) {
@@ -311,6 +327,26 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// The same two MMAs with descriptors given as SDesc words.
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, SDesc a, SDesc b, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+        "mov.b64 da, {%1, %2};\n\t"
+        "mov.b64 db, {%3, %4};\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+        "r"(a.lo), "r"(a.hi), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, SDesc b, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+        "mov.b64 db, {%2, %3};\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 // Arrives once on `bar` when every tcgen05 op issued so far by this thread is done.
