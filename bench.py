@@ -693,9 +693,13 @@ def main():
 
     # End to end through the public API with host buffers: every step copies its
     # inputs in from pinned host memory and reads every result back, inside the
-    # timing.  The copies run on their own streams and overlap the neighbouring
-    # steps' compute (device inputs and outputs double-buffered, events order the
-    # reuse of each buffer), as a training loop streaming its batches would run.
+    # timing.  Two schedules: the copies on their own streams, overlapping the
+    # neighbouring steps' compute (device inputs and outputs double-buffered,
+    # events order the reuse of each buffer), as a training loop streaming its
+    # batches would run; or in, compute, out one after another on one stream.
+    # Which is faster depends on the host link: where concurrent copies slow the
+    # kernels down more than they save, the serial one wins.  Both are tried for
+    # two steps and the faster one is timed.
     e2e = None
     if not args.no_e2e:
         # Pinned host buffers on the GPU's own NUMA node: pages are placed when
@@ -757,30 +761,49 @@ def main():
                     h_.copy_(d_, non_blocking=True)
             out_done[b].record(s_out)
 
-        def e2e_run(n_steps, t0=None, t1=None):
+        def e2e_run(n_steps, overlap, t0=None, t1=None):
             if t0 is not None:
                 t0.record(stream)
-            s_in.wait_stream(stream)
-            s_out.wait_stream(stream)
-            issue_in(0)
-            for n in range(n_steps):
-                if n + 1 < n_steps:
-                    issue_in(n + 1)
-                issue_comp(n)
-                issue_out(n)
-            stream.wait_stream(s_in)
-            stream.wait_stream(s_out)
+            if overlap:
+                s_in.wait_stream(stream)
+                s_out.wait_stream(stream)
+                issue_in(0)
+                for n in range(n_steps):
+                    if n + 1 < n_steps:
+                        issue_in(n + 1)
+                    issue_comp(n)
+                    issue_out(n)
+                stream.wait_stream(s_in)
+                stream.wait_stream(s_out)
+            else:
+                for n in range(n_steps):
+                    with torch.cuda.stream(stream):
+                        for d_, h_ in zip(xin[0], hin):
+                            d_.copy_(h_, non_blocking=True)
+                    in_ready[0].record(stream)
+                    issue_comp(0)
+                    with torch.cuda.stream(stream):
+                        for h_, d_ in zip(hout, yout[0]):
+                            h_.copy_(d_, non_blocking=True)
+                    out_done[0].record(stream)
             if t1 is not None:
                 t1.record(stream)
 
-        e2e_run(2)
-        torch.cuda.synchronize(dev)
+        trial = {}
+        for overlap in (True, False):
+            e2e_run(1, overlap)
+            torch.cuda.synchronize(dev)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e2e_run(2, overlap, a, b)
+            torch.cuda.synchronize(dev)
+            trial["overlapped" if overlap else "serial"] = max_over_ranks(a.elapsed_time(b), world) / 2
+        overlap = trial["overlapped"] <= trial["serial"]
         n_e2e = max(1, min(args.steps, 10))
         barrier(world)
         torch.cuda.synchronize(dev)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         comp_ev.clear()
-        e2e_run(n_e2e, a, b)
+        e2e_run(n_e2e, overlap, a, b)
         torch.cuda.synchronize(dev)
         barrier(world)
         dfa.dfa_check_errors(stream)
@@ -792,7 +815,9 @@ def main():
         bw = copy_bandwidth(hin, xin[1], hout, yout[1], s_in, s_out, dev)
         e2e = {"value": job_value(flops, e2e_ms, world), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": n_e2e,
-               "copies": "overlapped with the neighbouring steps' compute on two copy streams",
+               "copies": ("overlapped with the neighbouring steps' compute on two copy streams" if overlap else
+                          "in, compute, out one after another on the compute stream"),
+               "schedule_trial_ms": trial,
                "pinned_numa_node": node, **bw, "compute_ms_in_e2e": comp_ms,
                # a step costs at least max(compute, copies); the copies bound it when they take longer
                "link_bound": bw["both_ms"] > ms_step}

@@ -139,9 +139,11 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
 // mbar_wait.  For an MMA-issuing thread whose waits are usually short: a
 // suspended try_wait resumes a few hundred cycles after the phase completes,
 // which leaves the tensor pipe without queued work (measured on the backward:
-// about 5% of its time).
-__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err) {
-    if (mbar_test_wait(bar, parity)) return true;
+// about 5% of its time).  The first test is inline; the polling loop is out of
+// line (one copy per register budget R, as for mbar_wait_slow), which keeps the
+// issuing thread's code short: 0.7% on the backward against an inline loop.
+template <int R = 0>
+static __device__ __noinline__ bool mbar_spin_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err) {
     const uint64_t t0 = globaltimer();
     for (uint32_t i = 1;; ++i) {
         if (mbar_test_wait(bar, parity)) return true;
@@ -154,6 +156,11 @@ __device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, v
             }
         }
     }
+}
+template <int R = 0>
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err) {
+    if (mbar_test_wait(bar, parity)) return true;
+    return mbar_spin_slow<R>(bar, parity, abort_flag, err);
 }
 // Wait for the MMA issuer: a plain test first (the common case is a phase that
 // has already completed, and a potentially-suspending try_wait there leaves the
