@@ -327,10 +327,11 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         auto kmaj = [](int kk) -> uint32_t { return (uint32_t)(((kk / 4) * 16384 + (kk % 4) * 32) >> 4); };
         uint32_t n = 0, kvi = 0;
         bool ok = true;
-        uint64_t wt[4] = {0, 0, 0, 0};   // inputs (Q, dO, K/V, dK/dV free), dq_free, P^T, dS^T
         auto wait = [&](uint64_t* bar, uint32_t parity, int slot) {
-            ok = ok && (a.trace ? mbar_wait_acc(bar, parity, abort_flag, a.err, &wt[slot])
-                                : mbar_wait_spin(bar, parity, abort_flag, a.err));
+            // Not profiled, even when tracing: any profiling hook in this
+            // thread's waits (a pointer select, a traced branch) cost 1-2%.
+            ok = ok && mbar_wait_spin(bar, parity, abort_flag, a.err);
+            (void)slot;
             if (ok) tc_fence_after();
             return ok;
         };
@@ -407,7 +408,6 @@ bwd_pipe_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         mbar_wait(done, 0, &dummy, a.err);
         {
             trace_count(a.trace, a.trace_cap, 4, n);
-            for (int z = 0; z < 4; ++z) trace_wait(a.trace, a.trace_cap, 1 + z, wt[z]);
         }
     }
     tc_fence_before();
