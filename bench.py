@@ -133,8 +133,15 @@ class ClockSampler:
         mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in self.rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        pw = []
+        for r in self.rows:
+            try:
+                pw.append(float(r[3]))
+            except ValueError:
+                pass
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(self.rows)}
+                "reasons": reasons, "samples": len(self.rows),
+                "power_w": statistics.median(pw) if pw else None}
 
 
 def dist_setup(n_gpus, backend="nccl"):
@@ -803,8 +810,11 @@ def main():
         torch.cuda.synchronize(dev)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         comp_ev.clear()
+        e2e_clocks = ClockSampler(local if world > 1 else 0)
+        e2e_clocks.start()
         e2e_run(n_e2e, overlap, a, b)
         torch.cuda.synchronize(dev)
+        e2e_clk = e2e_clocks.stop()
         barrier(world)
         dfa.dfa_check_errors(stream)
         e2e_ms = max_over_ranks(a.elapsed_time(b), world) / n_e2e
@@ -819,6 +829,9 @@ def main():
                           "in, compute, out one after another on the compute stream"),
                "schedule_trial_ms": trial,
                "pinned_numa_node": node, **bw, "compute_ms_in_e2e": comp_ms,
+               # SM clock and board power while the end-to-end steps ran: host copies
+               # add power on a capped part, and the clock gives way
+               "clocks": e2e_clk,
                # a step costs at least max(compute, copies); the copies bound it when they take longer
                "link_bound": bw["both_ms"] > ms_step}
         del xin, yout
