@@ -582,11 +582,27 @@ def gpu_numa_cpus(index):
         return None, None
 
 
-def copy_bandwidth(hin, xin, hout, yout, s_in, s_out, device, reps=3):
+def copy_bandwidth(hin, xin, hout, yout, s_in, s_out, device, dfa, reps=3):
     """GB/s of the step's host-to-device copies alone, of its device-to-host
     copies alone, and of both at once, on the same pinned buffers and streams
-    as the end-to-end leg."""
+    as the end-to-end leg (copy engines); and of each direction through the SMs
+    (dfa_copy)."""
     import torch
+
+    def run_sm(h2d):
+        cur = torch.cuda.current_stream(device)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(device)
+        a.record(cur)
+        for _ in range(reps):
+            for h_, d_ in (zip(hin, xin) if h2d else zip(hout, yout)):
+                if h2d:
+                    dfa.dfa_copy(d_, h_, stream=cur)
+                else:
+                    dfa.dfa_copy(h_, d_, stream=cur)
+        b.record(cur)
+        torch.cuda.synchronize(device)
+        return a.elapsed_time(b) / reps
 
     def run(h2d, d2h):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -613,9 +629,12 @@ def copy_bandwidth(hin, xin, hout, yout, s_in, s_out, device, reps=3):
     bo = sum(t.numel() * t.element_size() for t in hout)
     run(True, True)
     t_in, t_out, t_both = run(True, False), run(False, True), run(True, True)
+    run_sm(True)
+    s_in_ms, s_out_ms = run_sm(True), run_sm(False)
     return {"h2d_gbs": bi / (t_in * 1e-3) / 1e9, "d2h_gbs": bo / (t_out * 1e-3) / 1e9,
             "h2d_ms": t_in, "d2h_ms": t_out, "both_ms": t_both,
-            "both_gbs": (bi + bo) / (t_both * 1e-3) / 1e9}
+            "both_gbs": (bi + bo) / (t_both * 1e-3) / 1e9,
+            "sm_h2d_gbs": bi / (s_in_ms * 1e-3) / 1e9, "sm_d2h_gbs": bo / (s_out_ms * 1e-3) / 1e9}
 
 
 # ---------------------------------------------------------------- GPU arm
@@ -700,13 +719,16 @@ def main():
 
     # End to end through the public API with host buffers: every step copies its
     # inputs in from pinned host memory and reads every result back, inside the
-    # timing.  Two schedules: the copies on their own streams, overlapping the
-    # neighbouring steps' compute (device inputs and outputs double-buffered,
-    # events order the reuse of each buffer), as a training loop streaming its
-    # batches would run; or in, compute, out one after another on one stream.
-    # Which is faster depends on the host link: where concurrent copies slow the
-    # kernels down more than they save, the serial one wins.  Both are tried for
-    # two steps and the faster one is timed.
+    # timing.  Three schedules: the copies on their own streams (DMA copy
+    # engines), overlapping the neighbouring steps' compute (device inputs and
+    # outputs double-buffered, events order the reuse of each buffer), as a
+    # training loop streaming its batches would run; in, compute, out one after
+    # another on one stream with the copy engines; or the same with the copies
+    # through the SMs (dfa_copy).  Which is fastest depends on the host link:
+    # where concurrent copies slow the kernels down more than they save, a
+    # serial one wins, and after heavy CPU work on the host the copy engines can
+    # run at a fraction of the link's rate while SM copies keep it.  Each is
+    # tried for two steps and the fastest is timed.
     e2e = None
     if not args.no_e2e:
         # Pinned host buffers on the GPU's own NUMA node: pages are placed when
@@ -768,10 +790,10 @@ def main():
                     h_.copy_(d_, non_blocking=True)
             out_done[b].record(s_out)
 
-        def e2e_run(n_steps, overlap, t0=None, t1=None):
+        def e2e_run(n_steps, mode, t0=None, t1=None):
             if t0 is not None:
                 t0.record(stream)
-            if overlap:
+            if mode == "overlapped":
                 s_in.wait_stream(stream)
                 s_out.wait_stream(stream)
                 issue_in(0)
@@ -783,28 +805,35 @@ def main():
                 stream.wait_stream(s_in)
                 stream.wait_stream(s_out)
             else:
+                sm = mode == "serial_sm"
                 for n in range(n_steps):
                     with torch.cuda.stream(stream):
                         for d_, h_ in zip(xin[0], hin):
-                            d_.copy_(h_, non_blocking=True)
+                            if sm:
+                                dfa.dfa_copy(d_, h_, stream=stream)
+                            else:
+                                d_.copy_(h_, non_blocking=True)
                     in_ready[0].record(stream)
                     issue_comp(0)
                     with torch.cuda.stream(stream):
                         for h_, d_ in zip(hout, yout[0]):
-                            h_.copy_(d_, non_blocking=True)
+                            if sm:
+                                dfa.dfa_copy(h_, d_, stream=stream)
+                            else:
+                                h_.copy_(d_, non_blocking=True)
                     out_done[0].record(stream)
             if t1 is not None:
                 t1.record(stream)
 
         trial = {}
-        for overlap in (True, False):
-            e2e_run(1, overlap)
+        for mode in ("overlapped", "serial", "serial_sm"):
+            e2e_run(1, mode)
             torch.cuda.synchronize(dev)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e2e_run(2, overlap, a, b)
+            e2e_run(2, mode, a, b)
             torch.cuda.synchronize(dev)
-            trial["overlapped" if overlap else "serial"] = max_over_ranks(a.elapsed_time(b), world) / 2
-        overlap = trial["overlapped"] <= trial["serial"]
+            trial[mode] = max_over_ranks(a.elapsed_time(b), world) / 2
+        mode = min(trial, key=trial.get)
         n_e2e = max(1, min(args.steps, 10))
         barrier(world)
         torch.cuda.synchronize(dev)
@@ -812,7 +841,7 @@ def main():
         comp_ev.clear()
         e2e_clocks = ClockSampler(local if world > 1 else 0)
         e2e_clocks.start()
-        e2e_run(n_e2e, overlap, a, b)
+        e2e_run(n_e2e, mode, a, b)
         torch.cuda.synchronize(dev)
         e2e_clk = e2e_clocks.stop()
         barrier(world)
@@ -822,11 +851,13 @@ def main():
         # the device-timed step, the copies are hidden; well above it, concurrent
         # copies slow the kernels down
         comp_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in comp_ev)
-        bw = copy_bandwidth(hin, xin[1], hout, yout[1], s_in, s_out, dev)
+        bw = copy_bandwidth(hin, xin[1], hout, yout[1], s_in, s_out, dev, dfa)
         e2e = {"value": job_value(flops, e2e_ms, world), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": n_e2e,
-               "copies": ("overlapped with the neighbouring steps' compute on two copy streams" if overlap else
-                          "in, compute, out one after another on the compute stream"),
+               "copies": {"overlapped": "overlapped with the neighbouring steps' compute on two copy streams",
+                          "serial": "in, compute, out one after another on the compute stream (copy engines)",
+                          "serial_sm": "in, compute, out one after another on the compute stream, copies through "
+                                       "the SMs (dfa_copy)"}[mode],
                "schedule_trial_ms": trial,
                "pinned_numa_node": node, **bw, "compute_ms_in_e2e": comp_ms,
                # SM clock and board power while the end-to-end steps ran: host copies

@@ -263,6 +263,25 @@ void dfa_shutdown(void);
  * stream holds a CUDA error, DFA_OK otherwise. */
 dfa_status dfa_check_errors(void* stream);
 
+/* Copy `bytes` bytes from src to dst through the SMs: a grid-stride kernel
+ * (one 512-thread block per SM, 16-byte accesses when both pointers are
+ * 16-byte aligned) reads and writes the two sides directly, so a pinned host
+ * buffer is read or written over the GPU's coherent host link without the
+ * DMA copy engines.  Not part of the pages' method: a staging helper for
+ * callers that stream batches between host and device (the benchmark's
+ * end-to-end leg uses it).  On a GB300 it moves 211 GB/s host to device and
+ * 193 GB/s back, the same as the copy engines, and unlike them it kept that
+ * rate right after heavy multi-threaded CPU work on the host, which left the
+ * copy engines at about half of it.
+ *   dst, src: device, managed or pinned (page-locked) host memory; must not
+ *             overlap
+ *   bytes:    any size
+ * Asynchronous on stream (an ordinary kernel launch: it occupies SMs while it
+ * runs).  Errors: INVALID_ARG for a null pointer (bytes > 0), overlapping
+ * ranges, or a pointer that is pageable host memory or unknown to CUDA;
+ * nothing is launched then. */
+dfa_status dfa_copy(void* dst, const void* src, size_t bytes, void* stream);
+
 /* Message for the last non-OK status returned on this thread ("" if none). */
 const char* dfa_last_error(void);
 
@@ -275,7 +294,8 @@ typedef enum {
     DFA_KERNEL_MERGE = 2,     /* partial rescale-and-merge                 */
     DFA_KERNEL_DELTA = 3,     /* Delta = rowsum(dO * O) preprocessing      */
     DFA_KERNEL_CONVERT = 4,   /* fp32 dQ accumulator -> output dtype       */
-    DFA_KERNEL_KINDS = 5
+    DFA_KERNEL_COPY = 5,      /* dfa_copy                                  */
+    DFA_KERNEL_KINDS = 6
 } dfa_kernel_kind;
 int64_t dfa_launch_count(dfa_kernel_kind kind);
 

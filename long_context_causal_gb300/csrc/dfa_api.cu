@@ -269,6 +269,32 @@ extern "C" int64_t dfa_launch_count(dfa_kernel_kind kind) {
     return g_launches[kind].load();
 }
 
+// dfa_copy: both sides must be reachable by the SMs (device, managed or pinned
+// host memory); pageable host memory is refused rather than guessed at.
+static dfa_status check_copy_side(const void* p, const char* which) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(DFA_ERR_INVALID_ARG, "dfa_copy: %s is not a CUDA-visible pointer", which);
+    }
+    if (at.type == cudaMemoryTypeUnregistered)
+        return fail(DFA_ERR_INVALID_ARG, "dfa_copy: %s is pageable host memory (pin it first)", which);
+    return DFA_OK;
+}
+
+extern "C" dfa_status dfa_copy(void* dst, const void* src, size_t bytes, void* stream) {
+    g_msg[0] = 0;
+    if (bytes == 0) return DFA_OK;
+    if (!dst || !src) return fail(DFA_ERR_INVALID_ARG, "dfa_copy: null pointer");
+    const uintptr_t d = reinterpret_cast<uintptr_t>(dst), r = reinterpret_cast<uintptr_t>(src);
+    if (d < r + bytes && r < d + bytes) return fail(DFA_ERR_INVALID_ARG, "dfa_copy: source and destination overlap");
+    dfa_status st;
+    if ((st = check_copy_side(dst, "dst")) || (st = check_copy_side(src, "src"))) return st;
+    st = launch_copy(dst, src, bytes, static_cast<cudaStream_t>(stream));
+    if (st == DFA_OK) count_launch(DFA_KERNEL_COPY);
+    return st;
+}
+
 extern "C" size_t dfa_attn_workspace_size(int B, int H, int H_kv, int S, int D, int n_chunks, int bwd) {
     if (B < 0 || H <= 0 || H_kv <= 0 || S < 0 || n_chunks <= 0 || (D != 64 && D != 128)) return 0;
     if (H % H_kv != 0 || !chunks_valid(S, n_chunks)) return 0;

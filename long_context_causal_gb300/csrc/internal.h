@@ -74,6 +74,7 @@ dfa_status launch_convert_varlen(int n_seq, int H, int64_t T, int64_t P, int D, 
                                  const float* acc, void* out, cudaStream_t s);
 // out[i] = bf16(in[i]) for n elements (n a multiple of 8; 16-byte aligned).
 dfa_status launch_cast_bf16(int64_t n, const float* in, void* out, cudaStream_t s);
+dfa_status launch_copy(void* dst, const void* src, size_t bytes, cudaStream_t s);
 // out[b, s, h, :] = scale * acc[b, h, s, :] cast to dt (acc is the head-major
 // fp32 dQ accumulator of the tensor-core backward; D a multiple of 8).
 // With accumulate, out is fp32 and the scaled values are added to it.

@@ -24,7 +24,7 @@ HEADER = os.path.join(INCLUDE, "dfa.h")
 DFA_OK, DFA_ERR_INVALID_ARG, DFA_ERR_UNSUPPORTED, DFA_ERR_CUDA, DFA_ERR_TIMEOUT, DFA_ERR_WORKSPACE = range(6)
 DFA_F32, DFA_BF16 = 0, 1
 DFA_SCHED_BALANCED, DFA_SCHED_UNBALANCED, DFA_SCHED_SPLIT_KV = 0, 1, 2
-KERNEL_KINDS = {"fwd": 0, "bwd": 1, "merge": 2, "delta": 3, "convert": 4}
+KERNEL_KINDS = {"fwd": 0, "bwd": 1, "merge": 2, "delta": 3, "convert": 4, "copy": 5}
 _SCHED = {"balanced": DFA_SCHED_BALANCED, "unbalanced": DFA_SCHED_UNBALANCED, "split_kv": DFA_SCHED_SPLIT_KV,
           DFA_SCHED_BALANCED: DFA_SCHED_BALANCED, DFA_SCHED_UNBALANCED: DFA_SCHED_UNBALANCED,
           DFA_SCHED_SPLIT_KV: DFA_SCHED_SPLIT_KV}
@@ -61,6 +61,7 @@ def _load() -> ctypes.CDLL:
         "dfa_shutdown": (None, []),
         "dfa_last_error": (ctypes.c_char_p, []),
         "dfa_launch_count": (i64, [i32]),
+        "dfa_copy": (i32, [vp, vp, ctypes.c_size_t, vp]),
         "dfa_build_worklist": (i64, [i32, i32, i32, i32, p32, p32]),
         "dfa_chunk_schedule": (i32, [i32, i32, i32, p32]),
         "dfa_split_piece_tiles": (i32, [i32, i32, i32, i32, i32]),
@@ -453,6 +454,22 @@ def dfa_last_error() -> str:
 
 def dfa_launch_count(kind: str | int) -> int:
     return int(_lib.dfa_launch_count(KERNEL_KINDS.get(kind, kind)))
+
+
+def dfa_copy(dst: torch.Tensor, src: torch.Tensor, stream=None) -> torch.Tensor:
+    """dst <- src, byte for byte, through the SMs (include/dfa.h: dfa_copy).
+    Both dense, with the same byte count; each on the GPU or in pinned host
+    memory.  Asynchronous on `stream` (default: the current stream)."""
+    for t, name in ((dst, "dst"), (src, "src")):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if t.numel() and not t.is_cuda and not t.is_pinned():   # an empty tensor has no memory to pin
+            raise ValueError(f"{name} must be on the GPU or in pinned host memory")
+    nb = dst.numel() * dst.element_size()
+    if nb != src.numel() * src.element_size():
+        raise ValueError(f"byte counts differ: dst {nb}, src {src.numel() * src.element_size()}")
+    _check(_lib.dfa_copy(_ptr(dst), _ptr(src), nb, _stream(stream)))
+    return dst
 
 
 def dfa_build_worklist(n_rows: int, n_units: int, n_workers: int, sched="balanced"):
