@@ -153,3 +153,26 @@ def test_the_full_size_checks_pass_exact_results_and_catch_a_wrong_head():
     bad[:, :, 3] = outs[2][:, :, 2]
     with pytest.raises(AssertionError, match="h3: dQ"):
         check_workload(w, True, q, k, v, do, outs[0], outs[1], bad, outs[3], outs[4])
+
+
+@pytest.mark.gpu
+def test_at_full_size_the_schedule_and_chunk_count_change_only_the_decomposition():
+    """The 128K workload as the benchmark runs it (balanced list, 16 chunks)
+    against the unbalanced list and against one chunk: the work decomposition
+    changes, the result does not.  O, lse, dK and dV are the same bits (every
+    output row is computed by one CTA in a fixed order); dQ adds fp32 partials
+    with atomics in no fixed order and may differ in its last bits."""
+    w = WORKLOADS["llama7b_s128k"]
+    q, k, v, do = make_workload(w, "cuda")
+    O, lse = dfa.dfa_attn_fwd(q, k, v, n_chunks=w.n_chunks, scale=w.scale, sched="balanced")
+    dQ, dK, dV = dfa.dfa_attn_bwd(q, k, v, O, lse, do, n_chunks=w.n_chunks, scale=w.scale, sched="balanced")
+    dq_max = dQ.float().abs().max().item()
+    for sched, P in (("unbalanced", w.n_chunks), ("balanced", 1)):
+        O2, l2 = dfa.dfa_attn_fwd(q, k, v, n_chunks=P, scale=w.scale, sched=sched)
+        assert torch.equal(O2, O) and torch.equal(l2, lse), (sched, P)
+        del O2, l2
+        g = dfa.dfa_attn_bwd(q, k, v, O, lse, do, n_chunks=P, scale=w.scale, sched=sched)
+        assert torch.equal(g[1], dK) and torch.equal(g[2], dV), (sched, P)
+        assert (g[0].float() - dQ.float()).abs().max().item() <= 1e-2 * dq_max, (sched, P)
+        del g
+    dfa.dfa_check_errors()
