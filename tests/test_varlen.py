@@ -150,3 +150,23 @@ def test_batches_of_empty_and_of_one_token_sequences():
     assert torch.max(torch.abs(dQ.float())).item() <= 1e-2 and torch.max(torch.abs(dK.float())).item() <= 1e-2
     dv_ref = do.float().view(7, 2, G, 128).sum(dim=2)
     assert torch.max(torch.abs(dV.float() - dv_ref)).item() <= 2e-2 * max(torch.max(torch.abs(dv_ref)).item(), 1.0)
+
+
+def test_the_benchmark_packed_batch_equals_one_dense_call_per_sequence():
+    """The packed batch the benchmark times (ten sequences, 57344 down to 512
+    tokens, 131072 in all, 32 heads, D = 128, same seed): one packed call each
+    way gives every sequence the bits of a dense call on that sequence alone
+    (O, lse, dK, dV), and its dQ within rounding."""
+    lens = [57344, 28672, 16384, 12288, 8192, 4096, 2048, 1024, 512, 512]
+    q, k, v, do, cu = packed(lens, 32, 32, 128, seed=5)
+    O, lse = dfa.dfa_attn_fwd_varlen(q, k, v, cu)
+    dQ, dK, dV = dfa.dfa_attn_bwd_varlen(q, k, v, O, lse, do, cu)
+    for a, b in zip(cu[:-1].tolist(), cu[1:].tolist()):
+        Od, ld = dfa.dfa_attn_fwd(q[None, a:b], k[None, a:b], v[None, a:b])
+        assert torch.equal(O[a:b], Od[0]) and torch.equal(lse[:, a:b], ld[0]), (a, b)
+        gq, gk, gv = dfa.dfa_attn_bwd(q[None, a:b], k[None, a:b], v[None, a:b], Od, ld, do[None, a:b])
+        assert torch.equal(dK[a:b], gk[0]) and torch.equal(dV[a:b], gv[0]), (a, b)
+        scale = gq.float().abs().max().item()
+        assert (dQ[a:b].float() - gq[0].float()).abs().max().item() <= 1e-2 * scale, (a, b)
+        del Od, ld, gq, gk, gv
+    dfa.dfa_check_errors()
