@@ -81,3 +81,39 @@ def test_bad_window_is_rejected():
     q, k, v, do = make(1, 2, 2, 256, 128, torch.bfloat16, device=DEV, seed=23)
     with pytest.raises(dfa.DfaError):
         dfa.dfa_attn_fwd_local(q, k, v, n_chunks=2, window=0)
+
+
+def test_the_benchmark_local_window_at_full_size():
+    """The configuration the benchmark times: the 128K workload (32 heads,
+    D = 128) in 16 chunks of 8192 tokens with a window of two chunks.  A query
+    row of chunk c sees exactly chunks c - 1 and c, and a key of chunk c - 1
+    is seen by the queries of chunks c - 1 and c; so the oracle's local window
+    on the slice of chunks [c - 2, c] (positions kept global through the
+    offsets) gives chunk c's O, lse and dQ and chunk c - 1's dK and dV as in
+    the whole sequence.  Checked for chunk 1 on head 0 and chunk 15 on the
+    last head (a different key/value head)."""
+    from long_context_causal_gb300.inputs import WORKLOADS, make_workload
+    w = WORKLOADS["llama7b_s128k"]
+    q, k, v, do = make_workload(w, DEV)
+    P, W = w.n_chunks, 2
+    C = w.S // P
+    O, lse = dfa.dfa_attn_fwd_local(q, k, v, n_chunks=P, window=W, scale=w.scale)
+    dQ, dK, dV = dfa.dfa_attn_bwd_local(q, k, v, O, lse, do, n_chunks=P, window=W, scale=w.scale)
+    dfa.dfa_check_errors()
+    for c, h in ((1, 0), (P - 1, w.H - 1)):
+        g = h // (w.H // w.H_kv)
+        a, m, b = max(c - 2, 0) * C, c * C, (c + 1) * C
+        prev = m - C - a                                  # chunk c - 1 within the slice
+        sl = lambda t, j: np64(t[:, a:b, j:j + 1])
+        Or, lr = oracle.attn_fwd_local(sl(q, h), sl(k, g), sl(v, g), chunk=C, window=W, scale=w.scale,
+                                       q_offset=a, kv_offset=a)
+        dqr, dkr, dvr = oracle.attn_bwd_local(sl(q, h), sl(k, g), sl(v, g), sl(do, h), chunk=C, window=W,
+                                              scale=w.scale, q_offset=a, kv_offset=a)
+        what = f"chunk {c} head {h}"
+        assert np.max(np.abs(np64(O[:, m:b, h]) - Or[:, m - a:, 0])) <= 2e-2, f"{what}: O"
+        assert np.max(np.abs(np64(lse[:, h, m:b]) - lr[:, 0, m - a:])) <= 1e-3, f"{what}: lse"
+        for name, gpu, ref in (("dQ", dQ[:, m:b, h], dqr[:, m - a:, 0]),
+                               ("dK", dK[:, m - C:m, g], dkr[:, prev:prev + C, 0]),
+                               ("dV", dV[:, m - C:m, g], dvr[:, prev:prev + C, 0])):
+            rel = np.max(np.abs(np64(gpu) - ref)) / max(np.max(np.abs(ref)), 1e-2)
+            assert rel <= 3e-2, f"{what}: {name} rel err {rel}"
