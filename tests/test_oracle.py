@@ -464,3 +464,31 @@ def test_varlen_rejects_bad_offsets():
     for cu in ([0, 3], [1, 4], [0, 3, 2, 4]):
         with pytest.raises(ValueError):
             oracle.attn_fwd_varlen(q, q, q, cu)
+
+
+def test_local_window_slices_reproduce_the_whole_sequence():
+    """With a window of two chunks, a query of chunk c sees chunks c - 1 and c
+    and a key of chunk c - 1 is seen by the queries of chunks c - 1 and c, so
+    the local window on the slice of chunks [c - 2, c] (offsets keeping the
+    positions global) gives chunk c's O, lse and dQ and chunk c - 1's dK and
+    dV exactly: the identity the full-size GPU check relies on."""
+    rng = np.random.default_rng(0)
+    S, D, C, W = 80, 8, 16, 2
+    q, k, v, do = (rng.standard_normal((1, S, 1, D)) for _ in range(4))
+    Of, lf = oracle.attn_fwd_local(q, k, v, chunk=C, window=W)
+    dqf, dkf, dvf = oracle.attn_bwd_local(q, k, v, do, chunk=C, window=W)
+    for c in range(1, S // C):
+        a, m, b = max(c - 2, 0) * C, c * C, (c + 1) * C
+        prev = m - C - a
+        Or, lr = oracle.attn_fwd_local(q[:, a:b], k[:, a:b], v[:, a:b], chunk=C, window=W, q_offset=a, kv_offset=a)
+        dqr, dkr, dvr = oracle.attn_bwd_local(q[:, a:b], k[:, a:b], v[:, a:b], do[:, a:b], chunk=C, window=W,
+                                              q_offset=a, kv_offset=a)
+        np.testing.assert_allclose(Or[:, m - a:], Of[:, m:b], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lr[:, :, m - a:], lf[:, :, m:b], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dqr[:, m - a:], dqf[:, m:b], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dkr[:, prev:prev + C], dkf[:, m - C:m], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dvr[:, prev:prev + C], dvf[:, m - C:m], rtol=0, atol=1e-12)
+        if c >= 2:   # the two-chunk slice is not enough: chunk c - 1's own queries lose chunk c - 2
+            _, dk2, _ = oracle.attn_bwd_local(q[:, m - C:b], k[:, m - C:b], v[:, m - C:b], do[:, m - C:b], chunk=C,
+                                              window=W, q_offset=m - C, kv_offset=m - C)
+            assert np.max(np.abs(dk2[:, :C] - dkf[:, m - C:m])) > 1e-3
