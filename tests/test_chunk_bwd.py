@@ -142,3 +142,58 @@ def test_bad_arguments_are_rejected():
         dfa.dfa_chunk_attn_bwd(q, k, v, O, lse, do, q_offset=-1)
     with pytest.raises(dfa.DfaError):
         dfa.dfa_chunk_attn_bwd(q, k, v, O, lse, do, workspace_buf=torch.empty(16, dtype=torch.uint8, device=DEV))
+
+
+def test_the_benchmark_chunk_steps_at_full_size():
+    """The chunk steps the benchmark times, on the 128K workload (16 chunks of
+    8192 tokens, 32 heads).  Forward: the last query chunk against key chunk 0
+    (no mask) and against itself (the diagonal) matches the oracle on sampled
+    rows of two heads, with the chunks' global offsets.  Backward: the chunk
+    steps of the last query chunk over all 16 key chunks add up to the
+    whole-sequence dQ of its rows, and those of key chunk 0 over all 16 query
+    chunks to the whole-sequence dK and dV of its keys (the whole-sequence
+    gradients are checked against the oracle at this size in
+    test_parity_large.py)."""
+    from long_context_causal_gb300.inputs import WORKLOADS, make_workload
+    w = WORKLOADS["llama7b_s128k"]
+    q, k, v, do = make_workload(w, DEV)
+    O, lse = dfa.dfa_attn_fwd(q, k, v, n_chunks=w.n_chunks, scale=w.scale)
+    dQ, dK, dV = dfa.dfa_attn_bwd(q, k, v, O, lse, do, n_chunks=w.n_chunks, scale=w.scale)
+    P = w.n_chunks
+    C = w.S // P
+    last = (P - 1) * C
+    G = w.H // w.H_kv
+    rng = np.random.default_rng(3)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, C - 1], rng.integers(0, C, 64)])).astype(np.int64)
+    idx = np.stack([np.zeros_like(rows), np.zeros_like(rows), rows], 1)
+    for ka in (0, last):
+        Op, lp = dfa.dfa_chunk_attn_fwd(q[:, last:], k[:, ka:ka + C], v[:, ka:ka + C], q_offset=last, kv_offset=ka,
+                                        scale=w.scale)
+        for h in (0, w.H - 1):
+            g = h // G
+            Or, lr = oracle.attn_fwd_rows(np64(q[:, last:, h:h + 1]), np64(k[:, ka:ka + C, g:g + 1]),
+                                          np64(v[:, ka:ka + C, g:g + 1]), idx, scale=w.scale, q_offset=last,
+                                          kv_offset=ka)
+            t = torch.as_tensor(rows, device=DEV)
+            assert np.max(np.abs(np64(Op[0, t, h]) - Or)) <= 2e-2, (ka, h, "O")
+            assert np.max(np.abs(np64(lp[0, h, t]) - lr)) <= 1e-3, (ka, h, "lse")
+        del Op, lp
+    f32 = dict(dtype=torch.float32, device=DEV)
+
+    def step(i, j, dq, dk, dv):
+        qs, ks = slice(i * C, (i + 1) * C), slice(j * C, (j + 1) * C)
+        dfa.dfa_chunk_attn_bwd(q[:, qs], k[:, ks], v[:, ks], O[:, qs], lse[:, :, qs].contiguous(), do[:, qs],
+                               q_offset=i * C, kv_offset=j * C, scale=w.scale, dQ_acc=dq, dK_acc=dk, dV_acc=dv)
+    dq = torch.zeros((1, C, w.H, w.D), **f32)
+    scratch_k, scratch_v = torch.zeros((1, C, w.H_kv, w.D), **f32), torch.zeros((1, C, w.H_kv, w.D), **f32)
+    for j in range(P):
+        step(P - 1, j, dq, scratch_k, scratch_v)
+    dk, dv = torch.zeros((1, C, w.H_kv, w.D), **f32), torch.zeros((1, C, w.H_kv, w.D), **f32)
+    scratch_q = torch.zeros((1, C, w.H, w.D), **f32)
+    for i in range(P):
+        step(i, 0, scratch_q, dk, dv)
+    dfa.dfa_check_errors()
+    for name, got, whole in (("dQ", dq, dQ[:, last:]), ("dK", dk, dK[:, :C]), ("dV", dv, dV[:, :C])):
+        ref = whole.float()
+        err = (got - ref).abs().max().item()
+        assert err <= 1e-2 * ref.abs().max().item(), f"{name}: {err}"
