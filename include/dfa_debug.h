@@ -35,7 +35,7 @@ dfa_status dfa_debug_mma(int form, const void* A, const void* B, float* C, void*
  *   softmax/compute thread processed, [8b + 6] = tiles its producer loaded,
  *   [8b + 7] = tiles its dQ drain warpgroup processed (backward; 0 forward),
  * and a wait profile at buf[8 capacity + 8b + slot]: SM clock cycles each
- * role spent blocked on barriers.  Backward slots: 0 producer (free slots),
+ * role spent blocked on barriers.  Backward slots: 0 P/dS warpgroup on dP^T,
  * 5 P/dS warpgroup on its tile inputs, 6 P/dS warpgroup on the dK/dV
  * accumulators, 7 dQ drain on the dQ MMA; slots 1-4 stay 0 (the MMA thread's
  * waits are not profiled: any hook in them slows the backward by 1-2%).

@@ -34,8 +34,12 @@
 // reduction: the next dP^T then waits for two TMEM loads, not for 64 KB of
 // reductions.  The registers for that come from a setmaxnreg split (the
 // control warpgroup needs few).
-// Trace wait slots (cycles): 0 P/dS dP^T, 1 MMA inputs, 2 MMA dq_free,
-// 3 MMA P^T done, 4 MMA dS^T done, 5 P/dS Q + S^T, 6 P/dS accumulators, 7 drain.
+// The MMA thread polls its barriers (bounded, loop out of line) and moves its
+// shared-memory descriptors with 32-bit adds on their low word: it shares its
+// sub-partition's issue slots with four busy warps, so every instruction it
+// saves per MMA shortens the tensor pipe's idle gaps.
+// Trace wait slots (cycles): 0 P/dS dP^T, 5 P/dS Q + S^T, 6 P/dS accumulators,
+// 7 drain; slots 1-4 stay 0 (the MMA thread's waits carry no trace hook).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
