@@ -270,9 +270,9 @@ dfa_status dfa_check_errors(void* stream);
  * DMA copy engines.  Not part of the pages' method: a staging helper for
  * callers that stream batches between host and device (the benchmark's
  * end-to-end leg uses it).  On a GB300 it moves 211 GB/s host to device and
- * 193 GB/s back, the same as the copy engines, and unlike them it kept that
- * rate right after heavy multi-threaded CPU work on the host, which left the
- * copy engines at about half of it.
+ * 193 GB/s back, the same as the copy engines.  Right after heavy
+ * multi-threaded CPU work on the host it kept 210 and 175 GB/s where the copy
+ * engines fell to 114 GB/s in (one box) or 67 GB/s out (another).
  *   dst, src: device, managed or pinned (page-locked) host memory; must not
  *             overlap
  *   bytes:    any size
